@@ -1,0 +1,206 @@
+"""Pins of the oracle's acceptance, compaction, drafter and speculative loop (CPU)."""
+import itertools
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import model as OM
+from oracle import spec as OS
+
+
+def _all_root_paths(parent, n_valid):
+    kids = {i: [j for j in range(1, n_valid) if parent[j] == i] for i in range(n_valid)}
+    out = []
+    def rec(p):
+        out.append(list(p))
+        for c in kids[p[-1]]:
+            rec(p + [c])
+    rec([0])
+    return out
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_accept_is_longest_matching_path(seed):
+    # In a real verification the prediction after a node depends only on the tokens of
+    # its root path, so duplicated siblings predict alike; model that with a hash of the
+    # path's tokens.  The walk then finds a longest root path whose every edge matches.
+    rng = np.random.default_rng(seed)
+    N = int(rng.integers(1, 17))
+    n_valid = int(rng.integers(1, N + 1))
+    V = 3                                                   # tiny vocab: many matches and duplicates
+    tok, parent = synth.random_tree(rng, N, V, n_valid=n_valid)
+    table = {}
+    def pred_of(i):
+        key = tuple(int(tok[j]) for j in OS.ancestors_or_self(parent, i))
+        if key not in table:
+            table[key] = int(rng.integers(0, V))
+        return table[key]
+    pred = [pred_of(i) for i in range(N)]
+    path, emitted = OS.accept(tok, parent, pred, n_valid)
+    ok = [p for p in _all_root_paths(parent, n_valid)
+          if all(tok[p[i + 1]] == pred[p[i]] for i in range(len(p) - 1))]
+    assert len(path) == max(len(p) for p in ok)
+    assert path in ok
+    assert emitted == [int(tok[j]) for j in path[1:]] + [pred[path[-1]]]
+    assert 1 <= len(emitted) <= n_valid
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_accept_walk_rule_arbitrary_predictions(seed):
+    # with arbitrary predictions: every step takes the lowest-index matching child, and
+    # the walk stops only where no valid child matches
+    rng = np.random.default_rng(1000 + seed)
+    N = int(rng.integers(1, 17))
+    n_valid = int(rng.integers(1, N + 1))
+    tok, parent = synth.random_tree(rng, N, 3, n_valid=n_valid)
+    pred = rng.integers(0, 3, size=N).tolist()
+    path, _ = OS.accept(tok, parent, pred, n_valid)
+    for a, b in zip(path, path[1:]):
+        match = [j for j in range(1, n_valid) if parent[j] == a and tok[j] == pred[a]]
+        assert b == min(match)
+    assert not [j for j in range(1, n_valid) if parent[j] == path[-1] and tok[j] == pred[path[-1]]]
+
+
+def test_accept_chain_is_longest_matching_prefix():
+    # a chain tree reduces to the linear rule: accept drafts while they equal the argmax
+    tok = [7, 1, 2, 3, 4]
+    parent = [-1, 0, 1, 2, 3]
+    pred = [1, 2, 9, 4, 5]
+    path, emitted = OS.accept(tok, parent, pred, 5)
+    assert path == [0, 1, 2] and emitted == [1, 2, 9]
+    path, emitted = OS.accept(tok, parent, [1, 2, 3, 4, 6], 5)
+    assert path == [0, 1, 2, 3, 4] and emitted == [1, 2, 3, 4, 6]     # full accept + bonus
+
+
+def test_compact_moves_path_rows():
+    w = OM.build_weights(synth.ModelShape("c", 1, 64, 4, 2, 16, 64, 64, 64, False), 1)
+    m = OM.Model(w, 12)
+    for l in range(1):
+        m.K[l][:] = np.arange(12, dtype=np.float32)[None, :, None]
+        m.V[l][:] = -np.arange(12, dtype=np.float32)[None, :, None]
+    OS.compact(m, 4, [0, 2, 5, 7])
+    assert m.K[0][0, :, 0].tolist() == [0, 1, 2, 3, 4, 6, 9, 11, 8, 9, 10, 11]
+    assert m.V[0][1, :, 3].tolist() == [-v for v in [0, 1, 2, 3, 4, 6, 9, 11, 8, 9, 10, 11]]
+
+
+def _brute_match(ctx, p, max_order=8):
+    best = 0
+    for l in range(1, max_order + 1):
+        if p - l + 1 < 0:
+            break
+        if ctx[p - l + 1:p + 1] == ctx[len(ctx) - l:]:
+            best = l
+    return best
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_match_lengths_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(0, 3, size=int(rng.integers(2, 60))).tolist()
+    ell = OS.match_lengths(ctx)
+    assert ell.tolist() == [_brute_match(ctx, p) for p in range(len(ctx) - 1)]
+
+
+def test_draft_single_candidate_is_prompt_lookup_chain():
+    # one earlier occurrence of the last token: the tree is the chain of its continuation
+    ctx = [10, 11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 10]
+    tok, parent, n_valid, best = OS.draft(ctx, 8)
+    assert best == 1 and n_valid == 8
+    assert tok.tolist() == [10, 11, 12, 13, 14, 15, 16, 17]
+    assert parent.tolist() == [-1, 0, 1, 2, 3, 4, 5, 6]
+    # continuation stops at 8 tokens and at the end of the context
+    tok, parent, n_valid, _ = OS.draft(ctx, 16)
+    assert n_valid == 9 and tok[1:9].tolist() == [11, 12, 13, 14, 15, 16, 17, 18]
+    assert tok[9:].tolist() == [0] * 7 and parent[9:].tolist() == [0] * 7
+
+
+def test_draft_no_match():
+    tok, parent, n_valid, best = OS.draft([1, 2, 3, 4], 4)
+    assert n_valid == 1 and best == 0 and tok[0] == 4
+
+
+def test_draft_scores_prefer_longer_matches():
+    # suffix "5 6" occurs twice: after "1 5 6" continues 7, after "2 5 6"... the longer match wins first
+    ctx = [9, 5, 6, 7, 1, 3, 5, 6, 8, 2, 9, 5, 6]
+    ell = OS.match_lengths(ctx)
+    assert ell[2] == 3 and ell[7] == 2
+    tok, parent, n_valid, best = OS.draft(ctx, 3)
+    assert best == 3
+    assert tok[1] == 7                     # continuation of the order-3 match has the larger score
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_draft_tree_is_prefix_closed_and_ordered(seed):
+    rng = np.random.default_rng(seed)
+    motifs = rng.integers(0, 20, size=(3, 6))
+    ctx = np.concatenate([motifs[i] for i in rng.integers(0, 3, size=12)]).tolist()
+    N = int(rng.integers(2, 17))
+    tok, parent, n_valid, best = OS.draft(ctx, N)
+    assert tok[0] == ctx[-1] and parent[0] == -1
+    for i in range(1, n_valid):
+        assert 0 <= parent[i] < i
+    # siblings are distinct tokens
+    for i in range(n_valid):
+        sib = [tok[j] for j in range(1, n_valid) if parent[j] == i]
+        assert len(sib) == len(set(sib))
+    # every root path of the tree is a continuation present in the context after a match
+    depth = OS.tree_depths(parent)
+    assert depth[:n_valid].max() <= 8
+
+
+def _weights():
+    return OM.build_weights(synth.TINY, 1000)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    w = _weights()
+    prompt = synth.motif_prompt(1001, 64, 4, 16, 0.1, synth.TINY.vocab)
+    greedy, _ = OM.greedy_decode(w, prompt, 32)
+    return w, prompt, greedy
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16])
+def test_speculative_equals_greedy(tiny, N):
+    w, prompt, greedy = tiny
+    out, stats = OS.spec_decode(w, prompt, 32, N)
+    assert out == greedy
+    for d, _best, n_valid in stats:
+        assert 0 <= d <= min(n_valid - 1, 8)
+
+
+def test_speculative_equals_greedy_with_varying_width(tiny):
+    w, prompt, greedy = tiny
+    widths = [1, 8, 2, 16, 4, 1, 3]
+    out, _ = OS.spec_decode(w, prompt, 32, lambda s: widths[s % len(widths)])
+    assert out == greedy
+
+
+def test_accepted_prefix_kv_equals_sequential_kv(tiny):
+    w, prompt, greedy = tiny
+    n = len(prompt)
+    rec = []
+    OS.spec_decode(w, prompt, 12, 8, record=rec)
+    # rebuild the spec model's cache state by replaying, then compare with a plain prefill
+    m = OM.Model(w, n + 64)
+    m.prefill(list(prompt[:-1]))
+    L_c = n - 1
+    for r in rec:
+        OS.tree_verify(m, L_c, r["tok"], r["parent"])
+        OS.compact(m, L_c, r["path"][:len(r["emitted"])])
+        L_c += len(r["emitted"])
+    seq = OM.Model(w, n + 64)
+    seq.prefill(list(prompt) + greedy[:L_c - n])
+    for l in range(synth.TINY.n_layers):
+        assert np.array_equal(m.K[l][:, :L_c], seq.K[l][:, :L_c])
+        assert np.array_equal(m.V[l][:, :L_c], seq.V[l][:, :L_c])
+
+
+def test_max_new_truncates_and_eos_stops(tiny):
+    w, prompt, greedy = tiny
+    out, _ = OS.spec_decode(w, prompt, 5, 16)
+    assert out == greedy[:5]
+    eos = greedy[3]
+    out, _ = OS.spec_decode(w, prompt, 32, 8, eos=eos)
+    assert out == greedy[:greedy.index(eos) + 1]
