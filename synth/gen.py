@@ -91,12 +91,19 @@ def normal(seed: int, stream: int, start: int, count: int, sigma: float) -> np.n
 
 
 def uniform_codes(seed: int, stream: int, start: int, count: int) -> np.ndarray:
-    """Uniform int4 codes in {-8..7} as int8."""
+    """Uniform int4 codes in {-8..7} as int8: element e is nibble e % 16 of word e // 16."""
     k = stream_key(seed, stream)
-    e = np.arange(start, start + count, dtype=np.uint64)
-    w = sm64(k, e // np.uint64(16))
-    nib = (w >> (np.uint64(4) * (e % np.uint64(16)))) & np.uint64(15)
-    return (nib.astype(np.int16) - 8).astype(np.int8)
+    w0, w1 = start // 16, (start + count + 15) // 16
+    out = np.empty((w1 - w0) * 16, dtype=np.int8)
+    shifts = (np.uint64(4) * np.arange(16, dtype=np.uint64))[None, :]
+    step = 1 << 20
+    for c0 in range(w0, w1, step):
+        c1 = min(w1, c0 + step)
+        w = sm64(k, np.arange(c0, c1, dtype=np.uint64))
+        nib = ((w[:, None] >> shifts) & np.uint64(15)).astype(np.int8) - np.int8(8)
+        out[(c0 - w0) * 16:(c1 - w0) * 16] = nib.reshape(-1)
+    off = start - w0 * 16
+    return out[off:off + count].copy()
 
 
 def uniform_scales(seed: int, stream: int, start: int, count: int,
