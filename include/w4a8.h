@@ -109,18 +109,235 @@ w4a8_status w4a8_quantize_rows(const float* x, int M, int K, int mode, int8_t* q
  * are folded left in ascending slice order; y = fold * s_a[t].
  *
  * a_q int8 [M][K], a_s fp32 [M] (device; per-token mode), w_t/s_t tiled layout
- * (device), y fp32 [M][N] (device, overwritten).  1 <= M <= 16, K % 32 == 0,
+ * (device, both 16-byte aligned), y fp32 [M][N] (device, overwritten).  1 <= M <= 16, K % 32 == 0,
  * N % 16 == 0.  workspace: device scratch of w4a8_matmul_workspace_bytes() bytes,
  * 256-byte aligned, owned by the caller, not shared by concurrent calls; its content
- * needs no initialisation.
+ * needs no initialisation (except for w4a8_matmul_check, below).  A bounded wait inside the
+ * kernel that expires makes the kernel skip its output and set the workspace status word.
  * ---------------------------------------------------------------------------- */
 w4a8_status w4a8_matmul_workspace_bytes(int M, int K, int N, size_t* bytes);
 w4a8_status w4a8_matmul(const int8_t* a_q, const float* a_s, int M, int K, const uint32_t* w_t,
                         const uint16_t* s_t, int N, float* y, void* workspace, size_t workspace_bytes,
                         void* stream);
 
+/* Host, synchronous.  Reads the device status word of a matmul workspace (call after the
+ * stream has finished).  *flags = 0 if every bounded pipeline wait of the kernels that
+ * used this workspace completed; otherwise bit 16 (timeout) is set and the call returns
+ * W4A8_ERR_DEVICE_FLAG.  The workspace must be zero-filled once before its first use for
+ * this word to be meaningful. */
+w4a8_status w4a8_matmul_check(const void* workspace, int M, int K, int N, uint32_t* flags);
+
 /* Number of K slices S that w4a8_matmul uses for a (K, N) shape (host). */
 int w4a8_matmul_slices(int K, int N);
+
+/* ==============================================================================
+ * Decoder, session and the GPU-resident speculation loop
+ * ============================================================================ */
+
+/* Shape of a Llama/Qwen-style decoder without biases, RMSNorm gain 1, rotate-half RoPE
+ * [P1 Experiments (models); Implementation].  hidden % 32 == 0, ffn % 32 == 0,
+ * (n_heads + 2 n_kv_heads) * head_dim % 16 == 0, head_dim in {64, 128},
+ * n_heads % n_kv_heads == 0, n_heads / n_kv_heads <= 8, vocab % 16 == 0. */
+typedef struct {
+  int n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
+  int tied;         /* 1: the LM head is the embedding table */
+  float rms_eps;    /* RMSNorm epsilon */
+  float rope_base;  /* RoPE base (theta_i = base^(-2i/head_dim)) */
+} w4a8_model_desc;
+
+/* Tensor kinds for w4a8_model_load_tensor; [rows][cols] of each (P2 layout, device):
+ *   Q [n_heads*head_dim][hidden], K and V [n_kv_heads*head_dim][hidden],
+ *   O [hidden][n_heads*head_dim], GATE and UP [ffn][hidden], DOWN [hidden][ffn],
+ *   EMBED and LM_HEAD [vocab][hidden] (LM_HEAD only when not tied). */
+enum {
+  W4A8_T_Q = 0, W4A8_T_K = 1, W4A8_T_V = 2, W4A8_T_O = 3, W4A8_T_GATE = 4, W4A8_T_UP = 5, W4A8_T_DOWN = 6,
+  W4A8_T_EMBED = 7, W4A8_T_LM_HEAD = 8
+};
+
+typedef struct w4a8_model w4a8_model;
+typedef struct w4a8_session w4a8_session;
+
+/* Host.  Allocates the model's device weight storage (tiled layout, fused QKV and
+ * GATE|UP matrices).  The weights must then be loaded with w4a8_model_load_tensor. */
+w4a8_status w4a8_model_create(const w4a8_model_desc* desc, w4a8_model** out);
+/* Device.  Copies one quantised tensor (P2 layout, device, caller-owned; may be freed
+ * after the stream has passed this call) into the model.  layer is ignored for EMBED and
+ * LM_HEAD. */
+w4a8_status w4a8_model_load_tensor(w4a8_model* m, int kind, int layer, const uint32_t* w_p2,
+                                   const uint16_t* s_p2, void* stream);
+/* Host.  Device bytes held by the model's weights. */
+w4a8_status w4a8_model_weight_bytes(const w4a8_model* m, size_t* bytes);
+void w4a8_model_destroy(w4a8_model* m);
+
+typedef struct {
+  int kv_cap;       /* KV slots per layer (>= prompt + max_new + max_width) */
+  int ctx_cap;      /* context token capacity (>= prompt + max_new + 9) */
+  int max_window;   /* largest window W of spec_window (1..64) */
+  int eos_id;       /* stop token, or -1 */
+} w4a8_session_desc;
+
+/* The 32-byte device control state [P1 GPU-Resident Speculation Loop]. */
+typedef struct {
+  uint32_t committed_len;  /* KV entries committed (all context tokens except the root) */
+  uint32_t ctx_len;        /* context tokens (prompt + generated); the last one is the root */
+  uint32_t n_valid;        /* valid nodes of the current full-width draft tree */
+  int32_t root_tok;        /* node 0 of the next step */
+  uint32_t n_generated;    /* tokens generated since the prompt */
+  uint32_t max_new;        /* generation stops at this many tokens */
+  uint32_t flags;          /* W4A8_FLAG_* */
+  uint32_t step_idx;       /* steps executed */
+} w4a8_ctl;
+
+/* The 16-byte host summary of the control state read between windows. */
+typedef struct {
+  uint32_t committed_len, n_generated, flags;
+  int32_t root_tok;
+} w4a8_ctl16;
+
+#define W4A8_FLAG_TERMINATED 1u     /* max_new reached or eos emitted */
+#define W4A8_FLAG_ERR_CAPACITY 2u   /* kv_cap or ctx_cap would be exceeded */
+#define W4A8_FLAG_ERR_TOKEN 4u      /* a token id outside [0, vocab) */
+#define W4A8_FLAG_ERR_TREE 8u       /* malformed tree */
+#define W4A8_FLAG_ERR_TIMEOUT 16u   /* a bounded device wait expired */
+
+/* Per-step statistics written by accept_greedy, 12 bytes [P1 GPU-Resident Speculation
+ * Loop; Feedback Control]: accepted draft nodes, match length of the drafter's best
+ * candidate, valid tree nodes, tokens emitted, low 32 bits of the device timer (ns) at
+ * the end of acceptance. */
+typedef struct {
+  uint16_t n_accepted_drafts, best_match_len, n_nodes, n_emitted;
+  uint32_t t_lo;
+} w4a8_step_stats;
+
+/* Host.  Allocates a session's device state (KV cache fp32 [layers][kv heads][kv_cap]
+ * [head_dim], context, control, activations, scratch) and pinned host mirrors. */
+w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc* desc, w4a8_session** out);
+void w4a8_session_destroy(w4a8_session* s);
+
+/* Device.  Starts a generation: context = prompt[0..n) (device int32), KV of
+ * prompt[0..n-1) computed through the verification kernels in chains of up to 16
+ * tokens, root = prompt[n-1], n_generated = 0, then the first draft tree. */
+w4a8_status w4a8_prefill(w4a8_session* s, const int32_t* prompt, int n, int max_new, void* stream);
+
+/* Device.  One verification pass over tree nodes 0..N-1 [P1 GPU-Resident Speculation
+ * Loop]: node i at logical position committed_len + depth(i) writes its K/V to slot
+ * committed_len + i and attends to cache slots [0, committed_len) and to its ancestors;
+ * pred[i] = argmax of its logits (lowest index on ties).  logits: optional device
+ * fp32 [N][vocab] copy of the logits (NULL = none).  1 <= N <= 16. */
+w4a8_status tree_verify_step(w4a8_session* s, int N, float* logits, void* stream);
+/* Device.  Greedy acceptance [P1; P3 section 4]: walks from the root following the
+ * lowest-index child whose token equals its parent's prediction; commits the accepted
+ * drafts and the bonus token (at most max_new - n_generated, stopping after eos); updates
+ * the control state, the context and the statistics. */
+w4a8_status accept_greedy(w4a8_session* s, int N, void* stream);
+/* Device.  Moves the accepted path's K/V rows to consecutive slots [P1; P3 section 7]. */
+w4a8_status kv_compact(w4a8_session* s, void* stream);
+/* Device.  Suffix n-gram drafter [P1 Draft-Free Drafting]: next tree of 16 nodes in
+ * best-first order (its first N nodes are the tree of width N). */
+w4a8_status ngram_draft(w4a8_session* s, void* stream);
+/* Device.  tree_verify_step + accept_greedy + kv_compact + ngram_draft. */
+w4a8_status w4a8_spec_step(w4a8_session* s, int N, void* stream);
+
+/* Device.  Launches W speculation steps of width N as one CUDA graph (captured on first
+ * use per (N, W)), followed by an asynchronous copy of the control state, the W step
+ * statistics and the emitted tokens into pinned host memory [P1 GPU-Resident Speculation
+ * Loop: windows of W steps, two windows in flight].  At most two windows may be in
+ * flight; the first call for a new (N, W) must not happen during stream capture. */
+w4a8_status spec_window(w4a8_session* s, int N, int W, void* stream);
+/* Host.  Waits (at most timeout_us microseconds; < 0 = no limit) for the oldest window in
+ * flight and returns its results: control summary, step statistics (*n_stats <= W) and
+ * emitted tokens (*n_tokens; tokens must hold 16 * W entries).  W4A8_ERR_TIMEOUT leaves the
+ * window in flight; W4A8_ERR_ARG if no window is in flight. */
+w4a8_status spec_poll(w4a8_session* s, w4a8_ctl16* ctl, w4a8_step_stats* stats, int* n_stats,
+                      int32_t* tokens, int* n_tokens, int64_t timeout_us);
+
+/* Host, synchronous.  Device-timed cost T(N) of one verification step plus drafting for
+ * each width [P1 Feedback Control: measured at load time], median of `trials` trials of
+ * `reps` back-to-back graph launches each; the session state is left unchanged. */
+w4a8_status w4a8_calibrate(w4a8_session* s, const int* widths, int n_widths, int reps, int trials,
+                           float* t_us);
+
+typedef struct {
+  int max_new;          /* tokens to generate */
+  int window;           /* W, steps per graph launch (1..max_window) */
+  int fixed_width;      /* > 0: every step uses this width; 0: the width controller */
+  int in_flight;        /* windows in flight (1 or 2) */
+  int64_t timeout_us;   /* per-window wait limit (< 0: none) */
+  int n_widths;         /* controller widths (ascending) and their costs T(N) in us */
+  int widths[8];
+  float t_us[8];
+} w4a8_decode_opts;
+
+typedef struct {
+  int n_tokens, n_steps, n_windows, host_syncs;
+  int accepted_drafts;  /* sum over steps */
+  int width_steps[17];  /* steps per width */
+  uint32_t flags;       /* final control flags */
+  double device_us;     /* device time from the first to the last step end */
+} w4a8_decode_report;
+
+/* Host, synchronous: the end-to-end call.  prompt: host int32[n_prompt]; out: host
+ * int32[max_new].  Copies the prompt to the device, prefills, then runs windows of
+ * speculation steps with `in_flight` windows in flight, choosing each window's width
+ * with the width controller (or fixed_width) between windows. */
+w4a8_status w4a8_decode(w4a8_session* s, const int32_t* prompt, int n_prompt, const w4a8_decode_opts* opts,
+                        int32_t* out, int* n_out, w4a8_decode_report* report, void* stream);
+
+/* Device.  ORs W4A8_FLAG_* bits into the control word between kernels: TERMINATED cancels
+ * the generation; an error bit makes every later kernel of the session a no-op (the host
+ * sees it in the next window's control summary).  Used for cancellation and for
+ * host-side fault injection in tests. */
+w4a8_status w4a8_session_raise_flags(w4a8_session* s, uint32_t flags, void* stream);
+
+/* Host, synchronous: the window loop of w4a8_decode on a session already prefilled by
+ * w4a8_prefill (the prompt and the KV cache stay resident on the device).  out: host
+ * int32[max_new of the prefill]; opts->max_new is ignored (the prefill fixed it). */
+w4a8_status w4a8_generate(w4a8_session* s, const w4a8_decode_opts* opts, int32_t* out, int* n_out,
+                          w4a8_decode_report* report, void* stream);
+
+/* Host, synchronous.  Device time of the matmul launches of one verification pass of
+ * width N (every layer and the LM head, nothing else) captured in one CUDA graph and
+ * replayed `reps` times: average microseconds per launch and average algorithmic bytes
+ * per launch (packed weights + scales + int8 activations + fp32 outputs). */
+w4a8_status w4a8_time_matmuls(w4a8_session* s, int N, int reps, double* us_per_launch, double* bytes_per_launch,
+                              int* launches_per_pass);
+
+/* Host, synchronous state access (tests and tools). */
+w4a8_status w4a8_session_get_ctl(w4a8_session* s, w4a8_ctl* ctl);
+/* Replaces the current tree: tok/parent host int32[n] with parent[0] = -1 and
+ * 0 <= parent[i] < i; nodes n..15 become padding. */
+w4a8_status w4a8_session_set_tree(w4a8_session* s, const int32_t* tok, const int32_t* parent, int n);
+w4a8_status w4a8_session_get_tree(w4a8_session* s, int32_t* tok, int32_t* parent, int32_t* depth, int* n_valid,
+                                  int* best_len);
+w4a8_status w4a8_session_get_pred(w4a8_session* s, int32_t* pred, int n);
+/* Copies the context tokens (host int32[cap]); *n = context length. */
+w4a8_status w4a8_session_get_context(w4a8_session* s, int32_t* out, int cap, int* n);
+/* Device.  Copies K and V of one layer, slots [slot0, slot0+n), into k_out/v_out (device
+ * fp32 [n_kv_heads][n][head_dim]). */
+w4a8_status w4a8_session_copy_kv(w4a8_session* s, int layer, int slot0, int n, float* k_out, float* v_out,
+                                 void* stream);
+
+/* ------------------------------------------------------------------------------
+ * Width controller [P1 Feedback Control of Speculation Width], host only.
+ * Chooses N maximising E[tokens per step | N] / T(N), where E is estimated from the
+ * recent best match lengths and the acceptance observed per (width, match length);
+ * probes a wider tree after a run of width-1 windows (spacing set by the costs);
+ * refines T(N) with an exponential moving average of the device-measured window
+ * completion intervals.
+ * ---------------------------------------------------------------------------- */
+typedef struct w4a8_controller w4a8_controller;
+w4a8_status w4a8_controller_create(const int* widths, const float* t_us, int n, w4a8_controller** out);
+void w4a8_controller_destroy(w4a8_controller* c);
+/* Width for the next window. */
+int w4a8_controller_choose(w4a8_controller* c);
+/* Feeds one finished window: its width, its step statistics and the device interval
+ * (us) since the previous window's end (<= 0: unknown). */
+w4a8_status w4a8_controller_observe(w4a8_controller* c, int width, const w4a8_step_stats* stats, int n,
+                                    double interval_us);
+/* Expected tokens per step of a width at the current statistics (for tests/reports). */
+double w4a8_controller_expected_tokens(const w4a8_controller* c, int width);
+/* Current cost estimate T(N) in us. */
+double w4a8_controller_cost(const w4a8_controller* c, int width);
 
 #ifdef __cplusplus
 }

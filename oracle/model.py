@@ -102,6 +102,21 @@ def quant_row(x: np.ndarray):
     return q[0], s[0]
 
 
+def decision_margin(x: np.ndarray) -> float:
+    """Distance, in code units, from the closest int8 decision of quant_row(x) to a rounding
+    boundary (k + 1/2).  A second evaluation whose inputs differ in the last bits can only
+    take a different code where this is small.  Diagnostic only."""
+    x32 = np.asarray(x, dtype=np.float32)
+    _, s = Q.quantize_act_per_token(x32[None, :])
+    if s[0] == 0:
+        return np.inf
+    r = np.abs(x32.astype(np.float64)) / np.float64(s[0])
+    r = r[r < 127.0]
+    if r.size == 0:
+        return np.inf
+    return float(np.min(np.abs(r - np.floor(r) - 0.5)))
+
+
 class Model:
     """A quantised decoder with an fp32 KV cache of ``kv_cap`` slots per layer."""
 
@@ -112,6 +127,9 @@ class Model:
         self.K = [np.zeros((sh.n_kv_heads, kv_cap, sh.head_dim), np.float32) for _ in range(sh.n_layers)]
         self.V = [np.zeros((sh.n_kv_heads, kv_cap, sh.head_dim), np.float32) for _ in range(sh.n_layers)]
         self._dq = {}
+        # diagnostic: smallest int8 decision margin of the token held in each cache slot
+        self.margin = np.full(kv_cap, np.inf)
+        self._m = np.inf
 
     # -- weights -----------------------------------------------------------
     def _deq(self, key, qs):
@@ -121,6 +139,7 @@ class Model:
 
     def linear(self, key, qs, x_row: np.ndarray) -> np.ndarray:
         """W4A8 product of one activation row: quantise, then the exact-operand fp64 product."""
+        self._m = min(self._m, decision_margin(x_row))
         q, s = quant_row(x_row)
         a = q.astype(np.float64) * np.float64(s)
         return self._deq(key, qs) @ a
@@ -140,9 +159,11 @@ class Model:
         n = len(toks)
         H, Hq, Hkv, d = sh.hidden, sh.n_heads, sh.n_kv_heads, sh.head_dim
         x = np.stack([self.embed(int(t)) for t in toks])
+        tok_m = np.full(n, np.inf)
         for l, Wl in enumerate(self.w.layers):
             qh = np.zeros((n, Hq, d))
             for i in range(n):
+                self._m = tok_m[i]
                 n1 = rmsnorm(x[i], sh.rms_eps)
                 qv = self.linear((l, synth.T_WQ), Wl[synth.T_WQ], n1).reshape(Hq, d)
                 kv = self.linear((l, synth.T_WK), Wl[synth.T_WK], n1).reshape(Hkv, d)
@@ -150,7 +171,9 @@ class Model:
                 qh[i] = rope(qv, int(pos[i]), sh.rope_base)
                 self.K[l][:, int(slots[i])] = rope(kv, int(pos[i]), sh.rope_base).astype(np.float32)
                 self.V[l][:, int(slots[i])] = vv.astype(np.float32)
+                tok_m[i] = self._m
             for i in range(n):
+                self._m = tok_m[i]
                 vis = np.asarray(visible[i], dtype=np.int64)
                 att = np.zeros((Hq, d))
                 for h in range(Hq):
@@ -163,9 +186,13 @@ class Model:
                     trace.setdefault("h", []).append(hrow.copy())
                     trace.setdefault("mlp", []).append(mlp.copy())
                 x[i] = hrow + mlp
+                tok_m[i] = self._m
         logits = np.zeros((n, sh.vocab))
         for i in range(n):
+            self._m = tok_m[i]
             logits[i] = self.linear("lm", self.w.lm_head, rmsnorm(x[i], sh.rms_eps))
+            tok_m[i] = self._m
+            self.margin[int(slots[i])] = tok_m[i]
         return logits
 
     def mlp(self, l, Wl, n2) -> np.ndarray:

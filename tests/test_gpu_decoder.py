@@ -1,0 +1,377 @@
+"""GPU decoder, speculation loop and windows against the oracle and the exactness invariants.
+
+The tiny decoder (2 layers, hidden 256, 4/2 heads of 64, FFN 688 padded to 704, vocab
+4096) is built twice from the same seeded stream: on the device by the library's own
+quantiser, and on the host by the oracle's.  Logit tolerance (per row): max |diff| <=
+2e-3 * (max - min of the oracle row); a greedy token must match wherever the oracle's
+top-2 margin exceeds twice that bound.
+
+Requantisation makes the logits sensitive to the last bit of the values that feed an
+int8 decision: once one code differs by one step, the difference reaches every later
+position through the KV cache (evaluating the same definition in fp32 instead of fp64,
+without any GPU, moves the logits after the 64-token prompt by up to 0.8% of their
+range).  The oracle records, for every token, the distance of its closest int8 decision
+to a rounding boundary.  A row must meet the 2e-3 bound whenever every decision in its
+dependency cone (the cached context and its ancestors) is at least DELTA = 2e-3 code units
+from a boundary -- far beyond the fp32 rounding of the kernels, so no code can differ;
+otherwise it must stay within 2e-2 of the range and its greedy token must agree where the
+margin allows.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import synth
+import synth.cuda as SC
+import w4a8_verify_gb300 as W
+from w4a8_verify_gb300 import models as WM
+from oracle import model as OM
+from oracle import spec as OS
+
+pytestmark = pytest.mark.gpu
+
+SHAPE = synth.TINY
+SEED = 1000
+REL_TOL = 2e-3
+REL_TOL_NEAR = 2e-2
+DELTA = 2e-3
+
+
+def _fill(shape, seed):
+    def fill(kind, layer, out):
+        if kind == W.T_EMBED:
+            SC.dense_weight(shape, seed, synth.STREAM_EMBED, shape.vocab, shape.hidden, shape.vocab, shape.hidden, out)
+        elif kind == W.T_LM_HEAD:
+            SC.dense_weight(shape, seed, synth.STREAM_LM_HEAD, shape.vocab, shape.hidden, shape.vocab, shape.hidden,
+                            out)
+        else:
+            rows, cols, rr, rc = synth.tensor_shape(shape, kind)
+            SC.dense_weight(shape, seed, synth.layer_stream(layer, kind), rows, cols, rr, rc, out)
+    return fill
+
+
+def gpu_model(shape=SHAPE, seed=SEED):
+    return WM.build_model(shape.n_layers, shape.hidden, shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.ffn,
+                          shape.vocab, shape.tied, _fill(shape, seed), shape.rms_eps, shape.rope_base)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    W.lib()
+    SC.lib()
+    m = gpu_model()
+    ow = OM.build_weights(SHAPE, SEED)
+    prompt = synth.motif_prompt(1001, 64, 4, 16, 0.1, SHAPE.vocab)
+    greedy, glogits = OM.greedy_decode(ow, prompt, 32)
+    return dict(model=m, ow=ow, prompt=prompt, greedy=greedy, glogits=glogits)
+
+
+def _session(t, kv_cap=256, ctx_cap=512, max_window=16, eos=-1):
+    return W.Session(t["model"], kv_cap, ctx_cap, max_window, eos)
+
+
+def _dev(a, dtype=torch.int32):
+    return torch.as_tensor(np.asarray(a), dtype=dtype).cuda()
+
+
+def _check_rows(gpu, ref, pred=None, rel=REL_TOL, near=None):
+    """Per-row tolerance and greedy-token agreement.  near[i]: row i depends on an int8
+    decision within DELTA of a rounding boundary (looser bound)."""
+    for i in range(ref.shape[0]):
+        rng = ref[i].max() - ref[i].min()
+        bound = (REL_TOL_NEAR if near is not None and near[i] else rel) * rng
+        err = np.abs(gpu[i].astype(np.float64) - ref[i]).max()
+        assert err <= bound, (i, err, bound)
+        if pred is not None:
+            top2 = np.sort(ref[i])[-2:]
+            if top2[1] - top2[0] > 2 * bound:
+                assert pred[i] == int(np.argmax(ref[i])), i
+
+
+def _forced_sequential_logits(t, tokens):
+    """GPU single-token steps over `tokens` (teacher-forced): logits after each token."""
+    s = _session(t)
+    s.prefill(_dev(tokens[:1]), max_new=len(tokens) + 4)
+    V = SHAPE.vocab
+    out = []
+    lg = torch.empty((1, V), dtype=torch.float32, device="cuda")
+    for j, tok in enumerate(tokens):
+        s.set_tree([int(tok)], [-1])
+        s.tree_verify_step(1, lg)
+        out.append(lg[0].clone())
+        s.accept_greedy(1)   # commits the root's K/V (L_c += 1)
+    torch.cuda.synchronize()
+    return torch.stack(out), s
+
+
+# ------------------------------------------------------------------------------ verify
+
+def _verify_case(tiny, prompt, tok, parent):
+    N = len(tok)
+    s = _session(tiny)
+    s.prefill(_dev(prompt), max_new=8)
+    s.set_tree(tok.tolist(), parent.tolist())
+    lg = torch.empty((N, SHAPE.vocab), dtype=torch.float32, device="cuda")
+    s.tree_verify_step(N, lg)
+    pred = s.pred(N)
+    L = len(prompt) - 1
+    m = OM.Model(tiny["ow"], len(prompt) + N + 1)
+    if L > 0:
+        m.prefill(list(prompt[:-1]))
+    ref = OS.tree_verify(m, L, tok, parent)
+    ctx_margin = m.margin[:L].min() if L > 0 else np.inf
+    near = [min(ctx_margin, min(m.margin[L + a] for a in OS.ancestors_or_self(parent, i))) < DELTA
+            for i in range(N)]
+    _check_rows(lg.cpu().numpy(), ref, pred, REL_TOL, near)
+    return sum(near)
+
+
+@pytest.mark.parametrize("seed,N,plen", [(0, 16, 32), (1, 8, 8), (2, 5, 16), (3, 1, 32), (4, 2, 9), (5, 16, 24),
+                                         (6, 11, 32), (7, 16, 1)])
+def test_tree_verify_matches_oracle(tiny, seed, N, plen):
+    rng = np.random.default_rng(seed)
+    prompt = synth.motif_prompt(2000 + seed, plen, 4, 8, 0.1, SHAPE.vocab)
+    tok, parent = synth.random_tree(rng, N, SHAPE.vocab)
+    _verify_case(tiny, prompt, tok, parent)
+
+
+@pytest.mark.parametrize("seed,N", [(0, 16), (1, 8), (2, 5)])
+def test_tree_verify_matches_oracle_after_64_token_prompt(tiny, seed, N):
+    rng = np.random.default_rng(seed)
+    tok, parent = synth.random_tree(rng, N, SHAPE.vocab)
+    _verify_case(tiny, tiny["prompt"], tok, parent)
+
+
+def test_verify_n_nodes_bitwise_equals_single_steps(tiny):
+    prompt = list(tiny["prompt"])
+    rng = np.random.default_rng(7)
+    N = 16
+    tok, parent = synth.random_tree(rng, N, SHAPE.vocab, max_depth=8)
+    s = _session(tiny)
+    s.prefill(_dev(prompt), max_new=8)
+    s.set_tree(tok.tolist(), parent.tolist())
+    lg = torch.empty((N, SHAPE.vocab), dtype=torch.float32, device="cuda")
+    s.tree_verify_step(N, lg)
+    torch.cuda.synchronize()
+    # each node against a teacher-forced single-token run over its root path
+    leaves = [i for i in range(N) if i not in set(parent.tolist())]
+    for leaf in leaves[:4]:
+        path = OS.ancestors_or_self(parent, leaf)
+        seq, _ = _forced_sequential_logits(tiny, prompt[:-1] + [int(tok[j]) for j in path])
+        for depth, node in enumerate(path):
+            assert torch.equal(lg[node], seq[len(prompt) - 1 + depth]), (leaf, node)
+
+
+def test_prefill_kv_bitwise_equals_sequential_kv(tiny):
+    prompt = list(tiny["prompt"])
+    s = _session(tiny)
+    s.prefill(_dev(prompt), max_new=8)
+    _, seq = _forced_sequential_logits(tiny, prompt[:-1])
+    n = len(prompt) - 1
+    shape = (SHAPE.n_kv_heads, n, SHAPE.head_dim)
+    for layer in range(SHAPE.n_layers):
+        k1, v1, k2, v2 = (torch.empty(shape, dtype=torch.float32, device="cuda") for _ in range(4))
+        s.copy_kv(layer, 0, n, k1, v1)
+        seq.copy_kv(layer, 0, n, k2, v2)
+        torch.cuda.synchronize()
+        assert torch.equal(k1, k2) and torch.equal(v1, v2)
+
+
+# ---------------------------------------------------------------------- accept / draft
+
+def test_first_draft_matches_oracle(tiny):
+    prompt = list(tiny["prompt"])
+    s = _session(tiny)
+    s.prefill(_dev(prompt), max_new=8)
+    tok, par, dep, n_valid, best = s.tree()
+    o_tok, o_par, o_nv, o_best = OS.draft(prompt, 16)
+    assert n_valid == o_nv and best == o_best
+    assert tok[:n_valid] == o_tok[:n_valid].tolist()
+    assert par[1:n_valid] == o_par[1:n_valid].tolist() and par[0] == -1
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_draft_matches_oracle_on_random_contexts(tiny, seed):
+    rng = np.random.default_rng(50 + seed)
+    n = int(rng.integers(2, 400))
+    motifs = rng.integers(0, 30, size=(4, 8))
+    ctx = np.concatenate([motifs[i] for i in rng.integers(0, 4, size=n // 8 + 1)])[:n].copy()
+    sub = rng.random(n) < 0.2
+    ctx[sub] = rng.integers(0, 30, size=int(sub.sum()))
+    s = _session(tiny, kv_cap=600, ctx_cap=1024)
+    s.prefill(_dev(ctx.astype(np.int32)), max_new=1)
+    tok, par, dep, n_valid, best = s.tree()
+    o_tok, o_par, o_nv, o_best = OS.draft(ctx.tolist(), 16)
+    assert (n_valid, best) == (o_nv, o_best)
+    assert tok[:n_valid] == o_tok[:n_valid].tolist() and par[1:n_valid] == o_par[1:n_valid].tolist()
+
+
+def test_spec_steps_match_oracle_loop(tiny):
+    """Step-by-step: the GPU's tree, acceptance and context follow the oracle's loop."""
+    prompt = list(tiny["prompt"])
+    rec = []
+    o_out, _ = OS.spec_decode(tiny["ow"], prompt, 24, 8, record=rec)
+    s = _session(tiny)
+    s.prefill(_dev(prompt), max_new=24)
+    for r in rec:
+        tok, par, dep, n_valid, best = s.tree()
+        nv = min(n_valid, 8)
+        assert nv == r["n_valid"] and tok[:nv] == r["tok"][:nv].tolist()
+        s.spec_step(8)
+        ctx = s.context()
+        assert ctx[len(prompt):] == o_out[:len(ctx) - len(prompt)]
+    assert s.context()[len(prompt):] == o_out
+
+
+# ------------------------------------------------------------------------- invariants
+
+@pytest.mark.parametrize("N,Wn", [(1, 1), (4, 1), (8, 4), (16, 16), (2, 3)])
+def test_speculative_equals_greedy_on_gpu(tiny, N, Wn):
+    prompt = list(tiny["prompt"])
+    s = _session(tiny)
+    greedy, rep_g = s.decode(prompt, 32, window=1, fixed_width=1, in_flight=1)
+    assert rep_g.host_syncs == rep_g.n_windows == 32
+    spec, rep = s.decode(prompt, 32, window=Wn, fixed_width=N, in_flight=2)
+    assert spec == greedy
+    assert rep.n_tokens == 32 and rep.flags & W.FLAG_TERMINATED
+    assert 1 <= 32 / rep.n_steps <= min(N, 9)
+
+
+def test_gpu_greedy_matches_oracle_greedy(tiny):
+    prompt = list(tiny["prompt"])
+    s = _session(tiny)
+    out, _ = s.decode(prompt, 32, window=4, fixed_width=8, in_flight=2)
+    ref, lg = tiny["greedy"], tiny["glogits"]
+    for i, (a, b) in enumerate(zip(out, ref)):
+        if a != b:
+            top2 = np.sort(lg[i])[-2:]
+            assert top2[1] - top2[0] <= 2 * REL_TOL * (lg[i].max() - lg[i].min()), i
+            break
+
+
+def test_accepted_prefix_kv_equals_sequential_kv(tiny):
+    prompt = list(tiny["prompt"])
+    s = _session(tiny)
+    out, _ = s.decode(prompt, 20, window=2, fixed_width=16, in_flight=2)
+    c = s.ctl()
+    L = c.committed_len
+    assert L == len(prompt) - 1 + len(out)
+    ref = _session(tiny)
+    ref.prefill(_dev(prompt + out), max_new=1)      # plain chains over the same tokens
+    shape = (SHAPE.n_kv_heads, L, SHAPE.head_dim)
+    for layer in range(SHAPE.n_layers):
+        k1, v1, k2, v2 = (torch.empty(shape, dtype=torch.float32, device="cuda") for _ in range(4))
+        s.copy_kv(layer, 0, L, k1, v1)
+        ref.copy_kv(layer, 0, L, k2, v2)
+        torch.cuda.synchronize()
+        assert torch.equal(k1, k2) and torch.equal(v1, v2)
+
+
+def test_controller_decode_equals_greedy(tiny):
+    prompt = list(tiny["prompt"])
+    s = _session(tiny)
+    greedy, _ = s.decode(prompt, 32, window=1, fixed_width=1, in_flight=1)
+    s.prefill(_dev(prompt), max_new=32)
+    widths = [1, 2, 4, 8, 16]
+    t = s.calibrate(widths, reps=5, trials=3)
+    assert all(v > 0 for v in t)
+    c = s.ctl()
+    assert c.committed_len == len(prompt) - 1 and c.n_generated == 0 and c.flags == 0
+    out, rep = s.decode(prompt, 32, window=2, fixed_width=0, widths=widths, t_us=t)
+    assert out == greedy
+    assert sum(rep.width_steps) == rep.n_steps
+
+
+def test_windows_and_poll(tiny):
+    prompt = list(tiny["prompt"])
+    s = _session(tiny)
+    greedy, _ = s.decode(prompt, 24, window=1, fixed_width=1, in_flight=1)
+    s.prefill(_dev(prompt), max_new=24)
+    s.spec_window(8, 3)
+    s.spec_window(4, 2)
+    with pytest.raises(W.W4A8Error):
+        s.spec_window(8, 1)                          # a third window in flight is refused
+    got = []
+    c, st, toks = s.spec_poll(3)
+    assert len(st) == 3 and sum(x.n_emitted for x in st) == len(toks)
+    got += toks
+    c, st, toks = s.spec_poll(2)
+    got += toks
+    while not (c.flags & W.FLAG_TERMINATED):
+        s.spec_window(16, 4)
+        c, st, toks = s.spec_poll(4)
+        got += toks
+    assert got == greedy
+    with pytest.raises(W.W4A8Error):
+        s.spec_poll(1)                               # nothing in flight
+
+
+def test_eos_stops_generation(tiny):
+    prompt = list(tiny["prompt"])
+    s = _session(tiny)
+    greedy, _ = s.decode(prompt, 32, window=1, fixed_width=1, in_flight=1)
+    eos = greedy[5]
+    s2 = _session(tiny, eos=eos)
+    out, rep = s2.decode(prompt, 32, window=4, fixed_width=8, in_flight=2)
+    assert out == greedy[:greedy.index(eos) + 1] and rep.flags & W.FLAG_TERMINATED
+
+
+# ------------------------------------------------------------------------- failures
+
+def test_capacity_overflow_is_reported_not_faulted(tiny):
+    prompt = list(tiny["prompt"])
+    s = _session(tiny, kv_cap=80, ctx_cap=512)
+    with pytest.raises(W.W4A8Error) as e:
+        s.decode(prompt, 32, window=4, fixed_width=8)      # 64 + 32 + 16 > 80: refused on the host
+    assert e.value.status == 4
+    out, rep = s.decode(prompt, 0, window=1, fixed_width=1)
+    assert out == [] and rep.flags & W.FLAG_TERMINATED
+
+
+def test_bad_trees_are_rejected(tiny):
+    s = _session(tiny)
+    s.prefill(_dev(list(tiny["prompt"])), max_new=4)
+    for tok, par in [([1, 2], [-1, 1]), ([1, 2], [0, 0]), ([1, 99999], [-1, 0]), ([1] * 17, [-1] + [0] * 16)]:
+        with pytest.raises(W.W4A8Error):
+            s.set_tree(tok, par)
+
+
+def test_steps_after_termination_are_noops(tiny):
+    prompt = list(tiny["prompt"])
+    s = _session(tiny)
+    s.prefill(_dev(prompt), max_new=16)
+    for _ in range(16):
+        s.spec_step(16)
+    c = s.ctl()
+    assert c.flags & W.FLAG_TERMINATED and c.n_generated == 16
+    s.spec_step(16)
+    c2 = s.ctl()
+    assert (c2.n_generated, c2.committed_len, c2.step_idx) == (c.n_generated, c.committed_len, c.step_idx)
+
+
+def test_raised_error_flag_stops_the_window(tiny):
+    """A flag raised between steps turns every later kernel of the session into a no-op."""
+    prompt = list(tiny["prompt"])
+    s = _session(tiny)
+    s.prefill(_dev(prompt), max_new=32)
+    s.spec_step(8)
+    c = s.ctl()
+    s.raise_flags(W.FLAG_ERR_TREE)
+    s.spec_window(8, 4)
+    c16, st, toks = s.spec_poll(4)
+    assert toks == [] and all(x.n_emitted == 0 for x in st)
+    assert c16.flags & W.FLAG_ERR_TREE and c16.n_generated == c.n_generated
+
+
+def test_cancel_by_terminate_flag(tiny):
+    prompt = list(tiny["prompt"])
+    s = _session(tiny)
+    s.prefill(_dev(prompt), max_new=32)
+    s.spec_step(4)
+    s.raise_flags(W.FLAG_TERMINATED)
+    n = s.ctl().n_generated
+    s.spec_step(4)
+    assert s.ctl().n_generated == n

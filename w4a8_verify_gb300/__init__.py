@@ -17,6 +17,44 @@ _lib = None
 
 _c = ctypes
 _vp, _i32, _u64, _sz, _f32, _i64 = _c.c_void_p, _c.c_int, _c.c_uint64, _c.c_size_t, _c.c_float, _c.c_int64
+_u16, _u32, _dbl = _c.c_uint16, _c.c_uint32, _c.c_double
+
+
+class ModelDesc(_c.Structure):
+    _fields_ = [("n_layers", _i32), ("hidden", _i32), ("n_heads", _i32), ("n_kv_heads", _i32), ("head_dim", _i32),
+                ("ffn", _i32), ("vocab", _i32), ("tied", _i32), ("rms_eps", _f32), ("rope_base", _f32)]
+
+
+class SessionDesc(_c.Structure):
+    _fields_ = [("kv_cap", _i32), ("ctx_cap", _i32), ("max_window", _i32), ("eos_id", _i32)]
+
+
+class Ctl(_c.Structure):
+    _fields_ = [("committed_len", _u32), ("ctx_len", _u32), ("n_valid", _u32), ("root_tok", _i32),
+                ("n_generated", _u32), ("max_new", _u32), ("flags", _u32), ("step_idx", _u32)]
+
+
+class Ctl16(_c.Structure):
+    _fields_ = [("committed_len", _u32), ("n_generated", _u32), ("flags", _u32), ("root_tok", _i32)]
+
+
+class StepStats(_c.Structure):
+    _fields_ = [("n_accepted_drafts", _u16), ("best_match_len", _u16), ("n_nodes", _u16), ("n_emitted", _u16),
+                ("t_lo", _u32)]
+
+
+class DecodeOpts(_c.Structure):
+    _fields_ = [("max_new", _i32), ("window", _i32), ("fixed_width", _i32), ("in_flight", _i32),
+                ("timeout_us", _i64), ("n_widths", _i32), ("widths", _i32 * 8), ("t_us", _f32 * 8)]
+
+
+class DecodeReport(_c.Structure):
+    _fields_ = [("n_tokens", _i32), ("n_steps", _i32), ("n_windows", _i32), ("host_syncs", _i32),
+                ("accepted_drafts", _i32), ("width_steps", _i32 * 17), ("flags", _u32), ("device_us", _dbl)]
+
+
+FLAG_TERMINATED, FLAG_ERR_CAPACITY, FLAG_ERR_TOKEN, FLAG_ERR_TREE, FLAG_ERR_TIMEOUT = 1, 2, 4, 8, 16
+T_Q, T_K, T_V, T_O, T_GATE, T_UP, T_DOWN, T_EMBED, T_LM_HEAD = range(9)
 
 # name -> argtypes (restype int = w4a8_status unless listed in _RESTYPE)
 _SIGNATURES = {
@@ -30,8 +68,45 @@ _SIGNATURES = {
     "w4a8_matmul_workspace_bytes": [_i32, _i32, _i32, _c.POINTER(_sz)],
     "w4a8_matmul": [_vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp],
     "w4a8_matmul_slices": [_i32, _i32],
+    "w4a8_matmul_check": [_vp, _i32, _i32, _i32, _c.POINTER(_c.c_uint32)],
+    "w4a8_model_create": [_c.POINTER(ModelDesc), _c.POINTER(_vp)],
+    "w4a8_model_load_tensor": [_vp, _i32, _i32, _vp, _vp, _vp],
+    "w4a8_model_weight_bytes": [_vp, _c.POINTER(_sz)],
+    "w4a8_model_destroy": [_vp],
+    "w4a8_session_create": [_vp, _c.POINTER(SessionDesc), _c.POINTER(_vp)],
+    "w4a8_session_destroy": [_vp],
+    "w4a8_prefill": [_vp, _vp, _i32, _i32, _vp],
+    "tree_verify_step": [_vp, _i32, _vp, _vp],
+    "accept_greedy": [_vp, _i32, _vp],
+    "kv_compact": [_vp, _vp],
+    "ngram_draft": [_vp, _vp],
+    "w4a8_spec_step": [_vp, _i32, _vp],
+    "spec_window": [_vp, _i32, _i32, _vp],
+    "spec_poll": [_vp, _c.POINTER(Ctl16), _c.POINTER(StepStats), _c.POINTER(_i32), _c.POINTER(_i32),
+                  _c.POINTER(_i32), _i64],
+    "w4a8_calibrate": [_vp, _c.POINTER(_i32), _i32, _i32, _i32, _c.POINTER(_f32)],
+    "w4a8_decode": [_vp, _c.POINTER(_i32), _i32, _c.POINTER(DecodeOpts), _c.POINTER(_i32), _c.POINTER(_i32),
+                    _c.POINTER(DecodeReport), _vp],
+    "w4a8_generate": [_vp, _c.POINTER(DecodeOpts), _c.POINTER(_i32), _c.POINTER(_i32), _c.POINTER(DecodeReport),
+                      _vp],
+    "w4a8_time_matmuls": [_vp, _i32, _i32, _c.POINTER(_dbl), _c.POINTER(_dbl), _c.POINTER(_i32)],
+    "w4a8_session_get_ctl": [_vp, _c.POINTER(Ctl)],
+    "w4a8_session_raise_flags": [_vp, _u32, _vp],
+    "w4a8_session_set_tree": [_vp, _c.POINTER(_i32), _c.POINTER(_i32), _i32],
+    "w4a8_session_get_tree": [_vp, _c.POINTER(_i32), _c.POINTER(_i32), _c.POINTER(_i32), _c.POINTER(_i32),
+                              _c.POINTER(_i32)],
+    "w4a8_session_get_pred": [_vp, _c.POINTER(_i32), _i32],
+    "w4a8_session_get_context": [_vp, _c.POINTER(_i32), _i32, _c.POINTER(_i32)],
+    "w4a8_session_copy_kv": [_vp, _i32, _i32, _i32, _vp, _vp, _vp],
+    "w4a8_controller_create": [_c.POINTER(_i32), _c.POINTER(_f32), _i32, _c.POINTER(_vp)],
+    "w4a8_controller_destroy": [_vp],
+    "w4a8_controller_choose": [_vp],
+    "w4a8_controller_observe": [_vp, _i32, _c.POINTER(StepStats), _i32, _dbl],
+    "w4a8_controller_expected_tokens": [_vp, _i32],
+    "w4a8_controller_cost": [_vp, _i32],
 }
-_RESTYPE = {"w4a8_status_str": _c.c_char_p}
+_RESTYPE = {"w4a8_status_str": _c.c_char_p, "w4a8_model_destroy": None, "w4a8_session_destroy": None,
+            "w4a8_controller_destroy": None, "w4a8_controller_expected_tokens": _dbl, "w4a8_controller_cost": _dbl}
 
 
 class W4A8Error(RuntimeError):
@@ -143,6 +218,15 @@ def w4a8_matmul_slices(K, N):
     return lib().w4a8_matmul_slices(K, N)
 
 
+def w4a8_matmul_check(workspace, M, K, N):
+    """Device status word of a matmul workspace (0 = every bounded wait completed)."""
+    f = _c.c_uint32()
+    st = lib().w4a8_matmul_check(_ptr(workspace), M, K, N, _c.byref(f))
+    if st not in (0, 7):
+        raise W4A8Error("w4a8_matmul_check", st)
+    return f.value
+
+
 def w4a8_matmul(a_q, a_s, w_t, s_t, N, y=None, workspace=None, stream=None):
     import torch
     M, K = a_q.shape
@@ -150,7 +234,208 @@ def w4a8_matmul(a_q, a_s, w_t, s_t, N, y=None, workspace=None, stream=None):
         y = torch.empty((M, N), dtype=torch.float32, device=a_q.device)
     need = w4a8_matmul_workspace_bytes(M, K, N)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=a_q.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=a_q.device)
     _call("w4a8_matmul", _ptr(a_q), _ptr(a_s), M, K, _ptr(w_t), _ptr(s_t), N, _ptr(y), _ptr(workspace),
           workspace.numel() * workspace.element_size(), _stream(stream))
     return y
+
+
+# ------------------------------------------------------------------------ model/session
+
+def _arr(vals, ctype=_i32):
+    vals = list(vals)
+    return (ctype * max(1, len(vals)))(*vals)
+
+
+class Model:
+    """A decoder held by the library (w4a8_model)."""
+
+    def __init__(self, n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab, tied,
+                 rms_eps=1e-6, rope_base=10000.0):
+        self.desc = ModelDesc(n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab, int(bool(tied)),
+                              rms_eps, rope_base)
+        h = _vp()
+        _call("w4a8_model_create", _c.byref(self.desc), _c.byref(h))
+        self.h = h
+
+    def load_tensor(self, kind, layer, w_p2, s_p2, stream=None):
+        _call("w4a8_model_load_tensor", self.h, int(kind), int(layer), _ptr(w_p2), _ptr(s_p2), _stream(stream))
+
+    def weight_bytes(self):
+        b = _sz()
+        _call("w4a8_model_weight_bytes", self.h, _c.byref(b))
+        return b.value
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().w4a8_model_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Session:
+    """A decoding session (w4a8_session) on a Model."""
+
+    def __init__(self, model, kv_cap, ctx_cap, max_window=16, eos_id=-1):
+        self.model = model
+        self.desc = SessionDesc(kv_cap, ctx_cap, max_window, eos_id)
+        h = _vp()
+        _call("w4a8_session_create", model.h, _c.byref(self.desc), _c.byref(h))
+        self.h = h
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().w4a8_session_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # device-side operations (asynchronous on the current stream)
+    def prefill(self, prompt_dev, max_new, stream=None):
+        _call("w4a8_prefill", self.h, _ptr(prompt_dev), int(prompt_dev.numel()), int(max_new), _stream(stream))
+
+    def tree_verify_step(self, N, logits=None, stream=None):
+        _call("tree_verify_step", self.h, int(N), _ptr(logits), _stream(stream))
+
+    def accept_greedy(self, N, stream=None):
+        _call("accept_greedy", self.h, int(N), _stream(stream))
+
+    def kv_compact(self, stream=None):
+        _call("kv_compact", self.h, _stream(stream))
+
+    def ngram_draft(self, stream=None):
+        _call("ngram_draft", self.h, _stream(stream))
+
+    def spec_step(self, N, stream=None):
+        _call("w4a8_spec_step", self.h, int(N), _stream(stream))
+
+    def spec_window(self, N, W, stream=None):
+        _call("spec_window", self.h, int(N), int(W), _stream(stream))
+
+    def spec_poll(self, W, timeout_us=-1):
+        c = Ctl16()
+        st = (StepStats * max(1, W))()
+        toks = (_i32 * (16 * max(1, W)))()
+        ns, nt = _i32(), _i32()
+        _call("spec_poll", self.h, _c.byref(c), st, _c.byref(ns), toks, _c.byref(nt), int(timeout_us))
+        return c, list(st)[:ns.value], list(toks)[:nt.value]
+
+    def calibrate(self, widths, reps=20, trials=5):
+        out = (_f32 * len(widths))()
+        _call("w4a8_calibrate", self.h, _arr(widths), len(widths), int(reps), int(trials), out)
+        return list(out)
+
+    @staticmethod
+    def _opts(max_new, window, fixed_width, in_flight, widths, t_us, timeout_us):
+        o = DecodeOpts()
+        o.max_new, o.window, o.fixed_width, o.in_flight, o.timeout_us = max_new, window, fixed_width, in_flight, timeout_us
+        o.n_widths = len(widths)
+        for i, (w, t) in enumerate(zip(widths, t_us)):
+            o.widths[i], o.t_us[i] = int(w), float(t)
+        return o
+
+    def generate(self, max_new, window=4, fixed_width=0, in_flight=2, widths=(), t_us=(), timeout_us=-1,
+                 stream=None):
+        """Window loop on a prefilled session; returns (tokens, DecodeReport)."""
+        o = self._opts(max_new, window, fixed_width, in_flight, widths, t_us, timeout_us)
+        out = (_i32 * max(1, max_new))()
+        n_out = _i32()
+        rep = DecodeReport()
+        _call("w4a8_generate", self.h, _c.byref(o), out, _c.byref(n_out), _c.byref(rep), _stream(stream))
+        return list(out)[:n_out.value], rep
+
+    def time_matmuls(self, N, reps=5):
+        us, by, nl = _dbl(), _dbl(), _i32()
+        _call("w4a8_time_matmuls", self.h, int(N), int(reps), _c.byref(us), _c.byref(by), _c.byref(nl))
+        return us.value, by.value, nl.value
+
+    def decode(self, prompt, max_new, window=4, fixed_width=0, in_flight=2, widths=(), t_us=(),
+               timeout_us=-1, stream=None):
+        """End-to-end decode from a host prompt; returns (tokens, DecodeReport)."""
+        o = DecodeOpts()
+        o.max_new, o.window, o.fixed_width, o.in_flight, o.timeout_us = max_new, window, fixed_width, in_flight, timeout_us
+        o.n_widths = len(widths)
+        for i, (w, t) in enumerate(zip(widths, t_us)):
+            o.widths[i], o.t_us[i] = int(w), float(t)
+        p = _arr([int(t) for t in prompt])
+        out = (_i32 * max(1, max_new))()
+        n_out = _i32()
+        rep = DecodeReport()
+        _call("w4a8_decode", self.h, p, len(prompt), _c.byref(o), out, _c.byref(n_out), _c.byref(rep),
+              _stream(stream))
+        return list(out)[:n_out.value], rep
+
+    def raise_flags(self, flags, stream=None):
+        _call("w4a8_session_raise_flags", self.h, int(flags), _stream(stream))
+
+    # synchronous state access
+    def ctl(self):
+        c = Ctl()
+        _call("w4a8_session_get_ctl", self.h, _c.byref(c))
+        return c
+
+    def set_tree(self, tok, parent):
+        n = len(tok)
+        _call("w4a8_session_set_tree", self.h, _arr(tok), _arr(parent), n)
+
+    def tree(self):
+        tok, par, dep = (_i32 * 16)(), (_i32 * 16)(), (_i32 * 16)()
+        nv, bl = _i32(), _i32()
+        _call("w4a8_session_get_tree", self.h, tok, par, dep, _c.byref(nv), _c.byref(bl))
+        return list(tok), list(par), list(dep), nv.value, bl.value
+
+    def pred(self, n):
+        out = (_i32 * n)()
+        _call("w4a8_session_get_pred", self.h, out, int(n))
+        return list(out)
+
+    def context(self, cap=1 << 16):
+        out = (_i32 * cap)()
+        n = _i32()
+        _call("w4a8_session_get_context", self.h, out, cap, _c.byref(n))
+        return list(out)[:min(cap, n.value)]
+
+    def copy_kv(self, layer, slot0, n, k_out, v_out, stream=None):
+        _call("w4a8_session_copy_kv", self.h, int(layer), int(slot0), int(n), _ptr(k_out), _ptr(v_out),
+              _stream(stream))
+
+
+class Controller:
+    """The host width controller (w4a8_controller)."""
+
+    def __init__(self, widths, t_us):
+        h = _vp()
+        _call("w4a8_controller_create", _arr(widths), _arr(t_us, _f32), len(widths), _c.byref(h))
+        self.h = h
+
+    def choose(self):
+        return lib().w4a8_controller_choose(self.h)
+
+    def observe(self, width, stats, interval_us=0.0):
+        arr = (StepStats * max(1, len(stats)))()
+        for i, st in enumerate(stats):
+            arr[i] = st if isinstance(st, StepStats) else StepStats(*st)
+        _call("w4a8_controller_observe", self.h, int(width), arr, len(stats), float(interval_us))
+
+    def expected_tokens(self, width):
+        return lib().w4a8_controller_expected_tokens(self.h, int(width))
+
+    def cost(self, width):
+        return lib().w4a8_controller_cost(self.h, int(width))
+
+    def __del__(self):
+        try:
+            if getattr(self, "h", None):
+                lib().w4a8_controller_destroy(self.h)
+                self.h = None
+        except Exception:
+            pass

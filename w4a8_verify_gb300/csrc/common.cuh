@@ -21,6 +21,17 @@
 
 namespace w4a8 {
 
+// Device error / state flags (the session control word and the matmul status word).
+enum : uint32_t {
+  FLAG_TERMINATED = 1u,
+  FLAG_ERR_CAPACITY = 2u,
+  FLAG_ERR_TOKEN = 4u,
+  FLAG_ERR_TREE = 8u,
+  FLAG_ERR_TIMEOUT = 16u,
+  FLAG_ERR_MASK = FLAG_ERR_CAPACITY | FLAG_ERR_TOKEN | FLAG_ERR_TREE | FLAG_ERR_TIMEOUT,
+  FLAG_STOP_MASK = FLAG_TERMINATED | FLAG_ERR_MASK,
+};
+
 static inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

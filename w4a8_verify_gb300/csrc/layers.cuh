@@ -1,0 +1,26 @@
+// Launchers of the decoder kernels (layers.cu) and the speculation kernels (spec.cu).
+#pragma once
+#include "decoder.cuh"
+
+namespace w4a8 {
+
+size_t attn_smem_bytes(int D, int Nq);
+cudaError_t attn_configure(int D, size_t smem);
+
+cudaError_t launch_embed(const DecoderBufs& b, const ModelDims& m, int N, const uint32_t* ew, const uint16_t* es,
+                         cudaStream_t st);
+cudaError_t launch_rmsnorm_quant(const DecoderBufs& b, const ModelDims& m, int N, cudaStream_t st);
+cudaError_t launch_rope_kv(const DecoderBufs& b, const ModelDims& m, int N, int layer, cudaStream_t st);
+cudaError_t launch_attention(const DecoderBufs& b, const ModelDims& m, int N, int layer, cudaStream_t st);
+cudaError_t launch_swiglu_quant(const DecoderBufs& b, const ModelDims& m, int N, cudaStream_t st);
+cudaError_t launch_argmax(const DecoderBufs& b, const ModelDims& m, int N, cudaStream_t st);
+
+// spec.cu
+cudaError_t launch_accept(const DecoderBufs& b, int N, int window_slot, cudaStream_t st);
+cudaError_t launch_compact(const DecoderBufs& b, const ModelDims& m, cudaStream_t st);
+cudaError_t launch_draft(const DecoderBufs& b, int force, cudaStream_t st);
+cudaError_t draft_configure(int ctx_cap);
+cudaError_t launch_chain_tree(const DecoderBufs& b, int start, int len, cudaStream_t st);
+cudaError_t launch_commit_chain(const DecoderBufs& b, int len, cudaStream_t st);
+
+}  // namespace w4a8

@@ -94,8 +94,10 @@ W4A8_API w4a8_status w4a8_weight_layout_bytes(int N, int K, size_t* words_bytes,
   return W4A8_OK;
 }
 
-// One thread per output word of the tiled layout (see layout.cuh).
-__global__ void k_repack_words(const uint32_t* __restrict__ wp2, int N, int K, uint32_t* __restrict__ wt) {
+// One thread per output word of the tiled layout (see layout.cuh).  The source rows
+// [0, N) land at rows [row0, row0 + N) of an Ntot-row tiled matrix.
+__global__ void k_repack_words(const uint32_t* __restrict__ wp2, int N, int K, int Ntot, int row0,
+                               uint32_t* __restrict__ wt) {
   griddep_wait();
   const long long total = (long long)tiled_words(N, K);
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -104,11 +106,11 @@ __global__ void k_repack_words(const uint32_t* __restrict__ wp2, int N, int K, u
   const int G = K / 32;
   const int j = (int)(i & 3);
   const int lane = (int)((i >> 2) & 31);
-  const long long rc = i >> 7;  // rb * KC + c
+  const long long rc = i >> 7;  // source (rb, c)
   const int c = (int)(rc % KC);
-  const long long rb = rc / KC;
+  const int rb = (int)(rc / KC);
   const int gid = lane >> 2, tig = lane & 3;
-  const long long row = rb * 16 + gid + ((j & 1) ? 8 : 0);
+  const long long row = (long long)rb * 16 + gid + ((j & 1) ? 8 : 0);
   const int g = 2 * c + (j >> 1);
   uint32_t out = 0x88888888u;  // code 0 in every nibble for a padding group
   if (g < G) {
@@ -122,10 +124,12 @@ __global__ void k_repack_words(const uint32_t* __restrict__ wp2, int N, int K, u
       out |= (n_lo | (n_hi << 4)) << (8 * b);
     }
   }
-  wt[i] = out;
+  const size_t t = tile_index(Ntot, KC, row0 / 16 + rb, c);
+  wt[t * 128 + (i & 127)] = out;
 }
 
-__global__ void k_repack_scales(const uint16_t* __restrict__ sp2, int N, int K, uint16_t* __restrict__ st) {
+__global__ void k_repack_scales(const uint16_t* __restrict__ sp2, int N, int K, int Ntot, int row0,
+                                uint16_t* __restrict__ st) {
   griddep_wait();
   const long long total = (long long)tiled_scales(N, K);
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -136,22 +140,34 @@ __global__ void k_repack_scales(const uint16_t* __restrict__ sp2, int N, int K, 
   const int gid = (int)((i >> 2) & 7);
   const long long rc = i >> 5;
   const int c = (int)(rc % KC);
-  const long long rb = rc / KC;
-  const long long row = rb * 16 + gid + ((j & 1) ? 8 : 0);
+  const int rb = (int)(rc / KC);
+  const long long row = (long long)rb * 16 + gid + ((j & 1) ? 8 : 0);
   const int g = 2 * c + (j >> 1);
-  st[i] = (g < G) ? sp2[row * G + g] : (uint16_t)0;
+  const size_t t = tile_index(Ntot, KC, row0 / 16 + rb, c);
+  st[t * 32 + (i & 31)] = (g < G) ? sp2[row * G + g] : (uint16_t)0;
 }
+
+namespace w4a8 {
+cudaError_t repack_run(const uint32_t* w_p2, const uint16_t* s_p2, int N, int K, int Ntot, int row0, uint32_t* w_t,
+                       uint16_t* s_t, cudaStream_t st) {
+  const long long nw = (long long)tiled_words(N, K), ns = (long long)tiled_scales(N, K);
+  cudaError_t e =
+      launch_pdl(k_repack_words, dim3((unsigned)((nw + 255) / 256)), dim3(256), 0, st, w_p2, N, K, Ntot, row0, w_t);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_repack_scales, dim3((unsigned)((ns + 255) / 256)), dim3(256), 0, st, s_p2, N, K, Ntot, row0,
+                    s_t);
+}
+}  // namespace w4a8
 
 W4A8_API w4a8_status w4a8_repack_weights(const uint32_t* w_p2, const uint16_t* s_p2, int N, int K,
                                          uint32_t* w_t, uint16_t* s_t, void* stream) {
   if (!w_p2 || !s_p2 || !w_t || !s_t || N <= 0 || K <= 0) return W4A8_ERR_ARG;
   if (N % 16 || K % 32) return W4A8_ERR_SHAPE;
-  if (!aligned(w_t, 16) || !aligned(s_t, 8)) return W4A8_ERR_ARG;
+  if (!aligned(w_t, 16) || !aligned(s_t, 16)) return W4A8_ERR_ARG;
   const long long nw = (long long)tiled_words(N, K), ns = (long long)tiled_scales(N, K);
   if ((nw + 255) / 256 > 0x7fffffffLL) return W4A8_ERR_SHAPE;
-  cudaStream_t st = as_stream(stream);
-  W4A8_CUDA_TRY(launch_pdl(k_repack_words, dim3((unsigned)((nw + 255) / 256)), dim3(256), 0, st, w_p2, N, K, w_t));
-  W4A8_CUDA_TRY(launch_pdl(k_repack_scales, dim3((unsigned)((ns + 255) / 256)), dim3(256), 0, st, s_p2, N, K, s_t));
+  (void)ns;
+  W4A8_CUDA_TRY(repack_run(w_p2, s_p2, N, K, N, 0, w_t, s_t, as_stream(stream)));
   return W4A8_OK;
 }
 
