@@ -83,6 +83,9 @@ struct DecoderBufs {
   float* kcache;          // [L][Hkv][kv_cap][D]
   float* vcache;
   float2* rope;           // [kv_cap][D/2] (cos, sin)
+  float2* qpart;          // [16][slices] (sum of squares, max |x|) partials of the quantisation passes
+  float2* argmax_part;    // [16][vocab slices] (value, index) partials
+  unsigned* argmax_tickets;  // [16], zero between kernels
   StepStats* wstats;      // [max_window] current window's statistics
   int32_t* wtok;          // [max_window][16] emitted tokens per step of the window
   int kv_cap, ctx_cap, n_chunks, max_window;

@@ -5,7 +5,7 @@
 namespace w4a8 {
 
 size_t attn_smem_bytes(int D, int Nq);
-cudaError_t attn_configure(int D, size_t smem);
+cudaError_t attn_configure(const ModelDims& m, size_t smem);
 
 cudaError_t launch_embed(const DecoderBufs& b, const ModelDims& m, int N, const uint32_t* ew, const uint16_t* es,
                          cudaStream_t st);

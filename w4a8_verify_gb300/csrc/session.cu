@@ -23,8 +23,6 @@
 using namespace w4a8;
 
 namespace {
-inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
-
 struct Arena {
   std::vector<void*> dev, host;
   ~Arena() {
@@ -308,6 +306,9 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
             A.dalloc(&b.a_s, kMaxWidth * 4) && A.dalloc(&b.mm_part, part * 4) && A.dalloc(&b.tickets, (size_t)tick * 4) &&
             A.dalloc(&b.kcache, kv) && A.dalloc(&b.vcache, kv) &&
             A.dalloc(&b.rope, (size_t)desc->kv_cap * (d.D / 2) * sizeof(float2)) &&
+            A.dalloc(&b.qpart, (size_t)kMaxWidth * (std::max({d.H, d.F, d.Hq * d.D}) / 512 + d.Hq + 2) * sizeof(float2)) &&
+            A.dalloc(&b.argmax_part, (size_t)kMaxWidth * ((d.V + 8191) / 8192) * sizeof(float2)) &&
+            A.dalloc(&b.argmax_tickets, kMaxWidth * 4) &&
             A.dalloc(&b.wstats, (size_t)desc->max_window * sizeof(StepStats)) &&
             A.dalloc(&b.wtok, (size_t)desc->max_window * kMaxWidth * 4) &&
             A.dalloc(&s->dev_rec, kRecBytesFixed + (size_t)desc->max_window * kRecStepBytes) &&
@@ -324,6 +325,7 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
   e = e == cudaSuccess ? cudaMemset(b.af, 0, afrag_uint4(Kmax) * 16) : e;
   e = e == cudaSuccess ? cudaMemset(b.corr, 0, corr_floats(Kmax) * 4) : e;
   e = e == cudaSuccess ? cudaMemset(b.tickets, 0, (size_t)tick * 4) : e;
+  e = e == cudaSuccess ? cudaMemset(b.argmax_tickets, 0, kMaxWidth * 4) : e;
   e = e == cudaSuccess ? cudaMemset(b.ctl, 0, sizeof(SpecCtl)) : e;
   e = e == cudaSuccess ? cudaMemset(b.rec, 0, sizeof(AcceptRec)) : e;
   e = e == cudaSuccess ? cudaMemset(b.tree, 0, sizeof(TreeState)) : e;
@@ -340,7 +342,7 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
   e = e == cudaSuccess ? cudaEventCreateWithFlags(&s->ev[0], cudaEventDisableTiming) : e;
   e = e == cudaSuccess ? cudaEventCreateWithFlags(&s->ev[1], cudaEventDisableTiming) : e;
   e = e == cudaSuccess ? cudaStreamCreateWithFlags(&s->cap, cudaStreamNonBlocking) : e;
-  e = e == cudaSuccess ? attn_configure(d.D, attn_smem_bytes(d.D, kMaxWidth * (d.Hq / d.Hkv))) : e;
+  e = e == cudaSuccess ? attn_configure(d, attn_smem_bytes(d.D, kMaxWidth * (d.Hq / d.Hkv))) : e;
   e = e == cudaSuccess ? mm_configure() : e;
   e = e == cudaSuccess ? draft_configure(desc->ctx_cap) : e;
   if (e != cudaSuccess) {
