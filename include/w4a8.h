@@ -127,6 +127,19 @@ w4a8_status w4a8_matmul(const int8_t* a_q, const float* a_s, int M, int K, const
  * this word to be meaningful. */
 w4a8_status w4a8_matmul_check(const void* workspace, int M, int K, int N, uint32_t* flags);
 
+/* Device.  The same product as w4a8_matmul (same kernels, same bits) for callers that
+ * cannot allocate device memory -- e.g. code already inside a CUDA stream capture, or hosts
+ * that give the library only its inputs and outputs.  It allocates nothing: its scratch is a
+ * 32 MiB array in the library's device image (held by every GPU that loads the library until
+ * the process exits); shapes whose scratch would exceed it return W4A8_ERR_CAPACITY before
+ * any launch.  The array's device address is looked up on the first call on each device, so
+ * that first call should come before any stream capture.  All calls share the array and it
+ * keeps the last call's contents (each call clears what must start at zero): calls that can
+ * overlap on the GPU (different streams, or threads without ordering) race and must not be
+ * issued.  The paper has no counterpart of this entry point. */
+w4a8_status w4a8_matmul_noalloc(const int8_t* a_q, const float* a_s, int M, int K, const uint32_t* w_t,
+                                const uint16_t* s_t, int N, float* y, void* stream);
+
 /* Number of K slices S that w4a8_matmul uses for a (K, N) shape (host). */
 int w4a8_matmul_slices(int K, int N);
 

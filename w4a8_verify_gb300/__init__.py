@@ -69,6 +69,7 @@ _SIGNATURES = {
     "w4a8_matmul": [_vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp],
     "w4a8_matmul_slices": [_i32, _i32],
     "w4a8_matmul_check": [_vp, _i32, _i32, _i32, _c.POINTER(_c.c_uint32)],
+    "w4a8_matmul_noalloc": [_vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp],
     "w4a8_model_create": [_c.POINTER(ModelDesc), _c.POINTER(_vp)],
     "w4a8_model_load_tensor": [_vp, _i32, _i32, _vp, _vp, _vp],
     "w4a8_model_weight_bytes": [_vp, _c.POINTER(_sz)],
@@ -225,6 +226,13 @@ def w4a8_matmul_check(workspace, M, K, N):
     if st not in (0, 7):
         raise W4A8Error("w4a8_matmul_check", st)
     return f.value
+
+
+def w4a8_matmul_noalloc(a_q, a_s, w_t, s_t, N, y, stream=None):
+    """w4a8_matmul with the library's own static scratch (no allocation; y is caller-owned)."""
+    M, K = a_q.shape
+    _call("w4a8_matmul_noalloc", _ptr(a_q), _ptr(a_s), M, K, _ptr(w_t), _ptr(s_t), N, _ptr(y), _stream(stream))
+    return y
 
 
 def w4a8_matmul(a_q, a_s, w_t, s_t, N, y=None, workspace=None, stream=None):
