@@ -75,8 +75,7 @@ struct DecoderBufs {
   float* logits;          // [16][V]
   float* o_part;          // [n_chunks][16][Hq][D]
   float* ml_part;         // [n_chunks][16][Hq][2]
-  uint4* af;              // activation fragments (max K)
-  float* corr;            // zero-point corrections
+  uint8_t* act;           // activation records of the next matmul (max K)
   float* a_s;             // [16] activation scales
   float* mm_part;         // split-K partials
   unsigned* tickets;      // split-K counters (zero between kernels)

@@ -92,7 +92,7 @@ __global__ void k_row_stats(const SpecCtl* ctl, const float* __restrict__ x, int
 // amax = max |x| * r, equal to the maximum of the rounded products since rounding is monotone).
 template <int MODE>
 __global__ void k_quant_slices(const SpecCtl* ctl, const float* __restrict__ x, int K, int ldx,
-                               const float2* __restrict__ part, int nparts, float eps, uint4* af, float* corr,
+                               const float2* __restrict__ part, int nparts, float eps, uint8_t* act, int M,
                                float* a_s) {
   griddep_wait();
   if (stopped(ctl)) return;
@@ -111,9 +111,10 @@ __global__ void k_quant_slices(const SpecCtl* ctl, const float* __restrict__ x, 
     for (int p = 0; p < nparts; ++p) mx = fmaxf(mx, part[(size_t)t * nparts + p].y);
   }
   const float s = __fdiv_rn(mx, 127.0f);
-  const int Gp = groups_padded(K);
+  const int NT = act_tiles(M);
   const int k = sl * kQuantSlice + 4 * threadIdx.x;
   const bool active = k < K;  // K % 32 == 0: groups of 8 lanes are all active or all idle
+  const bool pad = !active && k < chunks_of(K) * 64;  // the zero group that completes the last chunk
   uint32_t codes = 0;
   int sum = 0;
   if (active) {
@@ -127,12 +128,12 @@ __global__ void k_quant_slices(const SpecCtl* ctl, const float* __restrict__ x, 
       codes |= ((uint32_t)q & 0xffu) << (8 * b);
       sum += q;
     }
-    afrag_store_quad(af, Gp, t, k, codes);
   }
+  if (active || pad) act_store_quad(act, NT, t, k, codes);
   sum += __shfl_xor_sync(0xffffffffu, sum, 1);
   sum += __shfl_xor_sync(0xffffffffu, sum, 2);
   sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-  if (active && (threadIdx.x & 7) == 0) corr[(size_t)(k >> 5) * 16 + t] = (float)sum * -0.015625f;
+  if ((active || pad) && (threadIdx.x & 7) == 0) act_store_corr(act, NT, t, k >> 5, sum);
   if (sl == 0 && threadIdx.x == 0) a_s[t] = s;
 }
 
@@ -511,7 +512,7 @@ cudaError_t launch_rmsnorm_quant(const DecoderBufs& b, const ModelDims& m, int N
                              (const float*)b.x, m.H, b.qpart);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_quant_slices<1>, dim3(N, ns), dim3(kQuantSlice / 4), 0, st, (const SpecCtl*)b.ctl,
-                    (const float*)b.x, m.H, m.H, (const float2*)b.qpart, ns, m.eps, b.af, b.corr, b.a_s);
+                    (const float*)b.x, m.H, m.H, (const float2*)b.qpart, ns, m.eps, b.act, N, b.a_s);
 }
 
 cudaError_t launch_rope_kv(const DecoderBufs& b, const ModelDims& m, int N, int layer, cudaStream_t st) {
@@ -533,8 +534,8 @@ cudaError_t launch_attention(const DecoderBufs& b, const ModelDims& m, int N, in
   // the attention output (in the qkv buffer, [N][Hq*D]) -> int8 fragments of the O projection
   const int QD = m.Hq * m.D;
   return launch_pdl(k_quant_slices<0>, dim3(N, (QD + kQuantSlice - 1) / kQuantSlice), dim3(kQuantSlice / 4), 0, st,
-                    (const SpecCtl*)b.ctl, (const float*)b.qkv, QD, QD, (const float2*)b.qpart, m.Hq, 0.0f, b.af,
-                    b.corr, b.a_s);
+                    (const SpecCtl*)b.ctl, (const float*)b.qkv, QD, QD, (const float2*)b.qpart, m.Hq, 0.0f, b.act, N,
+                    b.a_s);
 }
 
 cudaError_t launch_swiglu_quant(const DecoderBufs& b, const ModelDims& m, int N, cudaStream_t st) {
@@ -543,7 +544,7 @@ cudaError_t launch_swiglu_quant(const DecoderBufs& b, const ModelDims& m, int N,
                              b.qpart);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_quant_slices<0>, dim3(N, ns), dim3(kQuantSlice / 4), 0, st, (const SpecCtl*)b.ctl,
-                    (const float*)b.gu, m.F, 2 * m.F, (const float2*)b.qpart, ns, 0.0f, b.af, b.corr, b.a_s);
+                    (const float*)b.gu, m.F, 2 * m.F, (const float2*)b.qpart, ns, 0.0f, b.act, N, b.a_s);
 }
 
 cudaError_t launch_argmax(const DecoderBufs& b, const ModelDims& m, int N, cudaStream_t st) {

@@ -1,23 +1,29 @@
-// The tiled weight layout and the activation fragment layout of the mma.sync matmul.
+// The tiled weight layout and the activation records of the mma.sync matmul.
 //
 // Tiled weights.  Rows form 16-row blocks rb; 16 consecutive blocks form a row group
 // (256 rows; the last group may hold fewer blocks, nrb).  Inside a row group the data is
 // ordered [64-input chunk c][block in group][...], so the K-range of a whole row group is
 // one contiguous byte range (one bulk copy per pipeline stage).  Per (rb, c):
 //   words  u32 [32 lanes][4]; lane = 4*gid + tig; word j holds row
-//          16*rb + gid + 8*(j&1) of group 2c + (j>>1); its byte b carries the code of
-//          input 32g + 4*tig + b in the low nibble and of input 32g + 16 + 4*tig + b in
-//          the high nibble, each stored as code + 8 (0..15).
+//          16*rb + gid + 8*(j&1) of group g = 2c + (j>>1).  Its nibble at bit 4p + 16h
+//          (p = 0..3, h = 0..1) carries the code of input 32g + 8p + 2*tig + h, stored as
+//          code + 8 (0..15).
 //   scales fp16 [8 gid][4] in the same (row, group) order as the words.
-// Masking a word with 0x0F0F0F0F (or shifting by 4 first) yields the four e4m3 bytes of
-// one m16n8k32 A-fragment register: the byte value n in 0..15 is the e4m3 encoding of
-// n * 2^-9 (subnormal below 8), so the MMA sees (q + 8) * 2^-9 exactly.
+// With x a word, the masks x & 0x000F000F, x & 0x00F000F0, (x>>8) & 0x000F000F and
+// (x>>8) & 0x00F000F0 are four f16x2 registers of m16n8k16 A fragments: the nibble n at
+// bits 0..3 (or 16..19) of a half is the subnormal f16 n * 2^-24, at bits 4..7 it is
+// 16n * 2^-24.  Pairs p = 1, 3 carry the extra factor 16, which the activation side
+// cancels by holding a/16 for those inputs.
 //
-// Activation fragments (layout [8-token tile nt][padded group g][lane]): uint4
-//   {hi(k0..k0+3), hi(k0+16..k0+19), lo(k0..k0+3), lo(k0+16..k0+19)}, k0 = 32g + 4*tig,
-//   token = 8*nt + gid, where an int8 a = 16*hi + lo and the bytes are e4m3 of 16*hi and
-//   of lo (exact).  corr[g][token] = -2^-6 * sum_{k in g} a (= -8 * sum a * 2^-9), the
-//   negated zero-point correction: sum (q+8) a - 8 sum a = sum q a.
+// Activation records.  For NT 8-token tiles (NT = 1 for up to 8 tokens, else 2) the
+// record of chunk c is NT * 1152 bytes at offset c * NT * 1152:
+//   [nt][group 0..1][lane] uint4 {h2(a_k, a_k+1), h2(a_k+8, a_k+9)/16,
+//                                h2(a_k+16, a_k+17), h2(a_k+24, a_k+25)/16},
+//        k = 32g + 2*tig, token 8*nt + gid (f16; a/16 is exact for an int8 a);
+//   [group 0..1][nt][tig] float4 {c(t0), c(t0+1), c(t0), c(t0+1)}, t0 = 8*nt + 2*tig,
+//        c(t) = -8 * 2^-24 * sum_{k in group} a_k(t), the zero-point correction that seeds
+//        the accumulator: sum (q+8) a 2^-24 - 8 sum a 2^-24 = sum q a 2^-24.
+// Tokens at or beyond the token count and inputs at or beyond K are zero.
 #pragma once
 #include <cstddef>
 
@@ -39,8 +45,9 @@ __host__ __device__ inline size_t tile_index(int N, int KC, int rb, int c) {
   return (size_t)grp * kGroupBlocks * KC + (size_t)c * nrb + rbl;
 }
 
-// activation fragment buffer (uint4 units) and correction floats for K inputs
-__host__ __device__ inline size_t afrag_uint4(int K) { return (size_t)groups_padded(K) * 2 * 32; }
-__host__ __device__ inline size_t corr_floats(int K) { return (size_t)groups_padded(K) * 16; }
+// activation records: 8-token tiles for M tokens, bytes per chunk, buffer bytes for K inputs
+__host__ __device__ inline int act_tiles(int M) { return M > 8 ? 2 : 1; }
+__host__ __device__ inline int act_rec_bytes(int NT) { return NT * 1152; }
+__host__ __device__ inline size_t act_bytes(int K) { return (size_t)chunks_of(K) * 2 * 1152; }
 
 }  // namespace w4a8

@@ -1,4 +1,4 @@
-// W4A8 small-batch matmul on the legacy tensor-core path (mma.sync m16n8k32 e4m3).
+// W4A8 small-batch matmul on the mma.sync tensor-core path (m16n8k16, f16 operands).
 //
 // "GPU-Resident Speculative Decoding ..." (Design > Small-Batch Verification Kernels):
 // verification multiplies every weight matrix by a handful of token vectors, so it
@@ -7,13 +7,17 @@
 // term.  Implementation (deterministic mode): the reduction order is fixed for every
 // token count, so N tokens give the bits of N single-token steps.
 //
-// GB300 design: the integer dot products run on the tensor cores instead of dp4a.
-// Weight codes n = q + 8 enter as e4m3 bytes n * 2^-9 (one AND per four codes), an int8
-// activation a enters as the exact pair (16*hi, lo) of e4m3 values, so every MMA
-// partial sum is an exact integer times 2^-9 and the group sum
-//   isum = 2^9 * (mma(n, 16hi) + mma(n, lo)) - 8 * sum(a)
-// is exact.  Each group's isum is scaled by its fp16 weight scale with one fmaf in a
-// fixed order; the schedule (slices of K) depends on (K, N) only.
+// GB300 design: the integer dot products run on the tensor cores.  A weight code
+// n = q + 8 enters as the subnormal f16 n * 2^-24 (one AND extracts two codes per
+// register), an int8 activation a as the f16 a (or a/16 where the code sits four bits
+// higher), so every product and every partial sum is an integer times 2^-24 well inside
+// the f32 mantissa: the group sum
+//   d = 2^-24 * (sum n a - 8 sum a) = 2^-24 * sum q a
+// is exact, the accumulator starting from the correction -8 * 2^-24 * sum a.  Each group's
+// d is scaled by its fp16 weight scale with one fmaf in a fixed order; the schedule
+// (slices of K) depends on (K, N) only.  (mma.sync with e4m3 operands would need the
+// same f16 tensor instructions plus conversions on this GPU; the f16 form feeds them
+// directly.)
 #include "matmul.cuh"
 
 namespace w4a8 {
@@ -21,7 +25,7 @@ namespace w4a8 {
 namespace {
 constexpr int kChunkBatch = 2;           // 64-input chunks per pipeline stage
 constexpr int kPersistentCtas = 304;     // fixed constant (2 x 152 SMs): part of the canonical schedule
-constexpr double kUnitFixedChunks = 3.0;  // modelled per-unit overhead, in chunk-streaming times
+constexpr double kUnitFixedChunks = 6.0;  // modelled per-unit overhead, in chunk-streaming times
 }  // namespace
 
 MatmulPlan mm_plan(int K, int N) {
@@ -53,54 +57,118 @@ MatmulPlan mm_plan(int K, int N) {
   return p;
 }
 
-// d = A * B + c, m16n8k32, e4m3 inputs, fp32 accumulation.
-__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1, float c0, float c1, float c2, float c3) {
-  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+// d = A * B + c, m16n8k16, f16 inputs, f32 accumulation.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1, float c0, float c1, float c2, float c3) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%10,%11,%12,%13};\n"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
 }
 
+// The four A-fragment registers of one weight word (see layout.cuh).
+__device__ __forceinline__ void unpack_codes(uint32_t x, uint32_t (&r)[4]) {
+  r[0] = x & 0x000F000Fu;
+  r[1] = x & 0x00F000F0u;
+  const uint32_t y = x >> 8;
+  r[2] = y & 0x000F000Fu;
+  r[3] = y & 0x00F000F0u;
+}
+
 constexpr int kRowBlocksPerCta = kWarpsPerCta * kRowBlocksPerWarp;   // 16
+static_assert(kChunkBatch == 2, "a stage holds one or two chunks");
 static_assert(kRowBlocksPerCta == kGroupBlocks, "a CTA covers one row group of the tiled layout");
-constexpr int kStageW = kRowBlocksPerCta * kChunkBatch * 512;         // weight bytes per stage
-constexpr int kStageS = kRowBlocksPerCta * kChunkBatch * 64;          // scale bytes per stage
-constexpr int kStageA = 2 * (2 * kChunkBatch) * 512;                  // fragment bytes (two 8-token tiles)
-constexpr int kStageC = (2 * kChunkBatch) * 64;                       // correction bytes
-constexpr int kStageBytes = kStageW + kStageS + kStageA + kStageC;
+// Shared-memory stage: weights [chunk][16 blocks][512 B], scales [chunk][16 blocks][64 B],
+// activation records [chunk][NT * 1152 B]; a row group with fewer blocks leaves a gap.
+constexpr int kChunkW = kRowBlocksPerCta * 512;
+constexpr int kChunkS = kRowBlocksPerCta * 64;
+constexpr int kStageS0 = kChunkBatch * kChunkW;
+constexpr int kStageA0 = kStageS0 + kChunkBatch * kChunkS;
+constexpr int kStageBytes = kStageA0 + kChunkBatch * 2 * 1152;
 constexpr int kStages = 4;
 constexpr int kMmThreads = 32 * (kWarpsPerCta + 1);                  // + one producer warp
 constexpr size_t kMmSmem = (size_t)kStages * kStageBytes;
 
+// NCH consecutive chunks of one stage for the kRowBlocksPerWarp row blocks from rl0.
+// Groups are folded into acc in ascending order.
+template <int NT, int NCH>
+__device__ __forceinline__ void mm_chunks(const uint8_t* stage, int u0, int rl0, int lane,
+                                          float (&acc)[kRowBlocksPerWarp][NT][4]) {
+  const int gid = lane >> 2, tig = lane & 3;
+  constexpr int rec = NT * 1152;
+#pragma unroll
+  for (int u = u0; u < u0 + NCH; ++u) {
+    const uint8_t* sa = stage + kStageA0 + u * rec;
+    uint4 bf[2][NT];
+    float4 cq[2][NT];
+#pragma unroll
+    for (int gg = 0; gg < 2; ++gg)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        bf[gg][nt] = reinterpret_cast<const uint4*>(sa + (nt * 2 + gg) * 512)[lane];
+        cq[gg][nt] = reinterpret_cast<const float4*>(sa + NT * 1024 + (gg * NT + nt) * 64)[tig];
+      }
+#pragma unroll
+    for (int r = 0; r < kRowBlocksPerWarp; ++r) {
+      const int rl = rl0 + r;
+      const uint4 wv = reinterpret_cast<const uint4*>(stage + u * kChunkW + rl * 512)[lane];
+      const uint2 sv = reinterpret_cast<const uint2*>(stage + kStageS0 + u * kChunkS + rl * 64)[gid];
+      float2 sg[2];
+      sg[0] = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));  // (row gid, row gid+8), group 0
+      sg[1] = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));
+      uint32_t wa[2][4], wb[2][4];  // [group][register] of rows gid and gid+8
+      unpack_codes(wv.x, wa[0]);
+      unpack_codes(wv.y, wb[0]);
+      unpack_codes(wv.z, wa[1]);
+      unpack_codes(wv.w, wb[1]);
+      float d[2][NT][4];
+#pragma unroll
+      for (int gg = 0; gg < 2; ++gg)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_f16(d[gg][nt], wa[gg][0], wb[gg][0], wa[gg][1], wb[gg][1], bf[gg][nt].x, bf[gg][nt].y,
+                  cq[gg][nt].x, cq[gg][nt].y, cq[gg][nt].z, cq[gg][nt].w);
+#pragma unroll
+      for (int gg = 0; gg < 2; ++gg)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_f16(d[gg][nt], wa[gg][2], wb[gg][2], wa[gg][3], wb[gg][3], bf[gg][nt].z, bf[gg][nt].w,
+                  d[gg][nt][0], d[gg][nt][1], d[gg][nt][2], d[gg][nt][3]);
+#pragma unroll
+      for (int gg = 0; gg < 2; ++gg)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          acc[r][nt][0] = fmaf(sg[gg].x, d[gg][nt][0], acc[r][nt][0]);
+          acc[r][nt][1] = fmaf(sg[gg].x, d[gg][nt][1], acc[r][nt][1]);
+          acc[r][nt][2] = fmaf(sg[gg].y, d[gg][nt][2], acc[r][nt][2]);
+          acc[r][nt][3] = fmaf(sg[gg].y, d[gg][nt][3], acc[r][nt][3]);
+        }
+    }
+  }
+}
+
 // Persistent CTAs: kWarpsPerCta consumer warps (kRowBlocksPerWarp 16-row blocks each) and one
 // producer warp.  Work units (row group g, K slice s), unit w = g*S + s, are dealt round-robin to
 // the CTAs.  The producer streams, per stage of kChunkBatch 64-input chunks, the row group's
-// weights and scales, the activation fragments and the zero-point corrections into a
-// kStages-deep shared-memory ring with cp.async.bulk, continuing across units; weight copies of
-// the first stages are issued before griddepcontrol.wait (weights are constant), activations
-// only after it.  A unit's result is folded with the other slices of its row group by the last
-// unit to finish (ticket), in ascending slice order.
+// weights and scales and the activation records into a kStages-deep shared-memory ring with
+// cp.async.bulk, continuing across units; weight copies of the first stages are issued before
+// griddepcontrol.wait (weights are constant), activations only after it.  A unit's result is
+// folded with the other slices of its row group by the last unit to finish (ticket), in
+// ascending slice order.
 template <int NT>
 __global__ void __launch_bounds__(kMmThreads)
-    k_mm(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ st, const uint8_t* __restrict__ af,
-         const uint8_t* __restrict__ corr, const float* __restrict__ a_s, int M, int N, int ldy, int KC, int cps,
-         int S, float* __restrict__ y, int epi, float* __restrict__ part, unsigned* __restrict__ tickets,
-         unsigned* __restrict__ err, const unsigned* __restrict__ stop) {
+    k_mm(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ st, const uint8_t* __restrict__ act,
+         const float* __restrict__ a_s, int M, int N, int ldy, int KC, int cps, int S, float* __restrict__ y,
+         int epi, float* __restrict__ part, unsigned* __restrict__ tickets, unsigned* __restrict__ err,
+         const unsigned* __restrict__ stop) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full[kStages], empty[kStages];
   __shared__ unsigned s_ticket;
+  constexpr int rec = NT * 1152;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n16 = N / 16;
-  const int Gp = 2 * KC;  // padded groups
   const int n_rg = (n16 + kGroupBlocks - 1) / kGroupBlocks;
   const int units = n_rg * S;
-  // batches of unit w (the slice's chunk range split into stages)
-  auto unit_batches = [&](int w) {
-    const int sl = w % S;
-    const int c0 = sl * cps, c1 = min(KC, c0 + cps);
-    return (c1 - c0 + kChunkBatch - 1) / kChunkBatch;
-  };
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
@@ -115,10 +183,10 @@ __global__ void __launch_bounds__(kMmThreads)
   if (warp == kWarpsPerCta) {
     // ---------------- producer ----------------
     if (lane == 0) {
-      // batch sequence of this CTA: units blockIdx.x, +gridDim.x, ...; each unit's batches
       struct Pos {
         int w, b;
       };
+      // stage `ps`: row group g, first chunk cb, nc chunks, nrb row blocks
       auto batch_info = [&](Pos ps, int& g, int& cb, int& nc, int& nrb) {
         const int sl = ps.w % S;
         g = ps.w / S;
@@ -128,28 +196,35 @@ __global__ void __launch_bounds__(kMmThreads)
         nrb = min(kGroupBlocks, n16 - g * kGroupBlocks);
       };
       auto next = [&](Pos ps) {
-        if (ps.b + 1 < unit_batches(ps.w)) return Pos{ps.w, ps.b + 1};
+        const int sl = ps.w % S;
+        const int c0 = sl * cps, c1 = min(KC, c0 + cps);
+        if (c0 + (ps.b + 1) * kChunkBatch < c1) return Pos{ps.w, ps.b + 1};
         return Pos{ps.w + (int)gridDim.x, 0};
       };
       auto issue_weights = [&](Pos ps, int it) {
         int g, cb, nc, nrb;
         batch_info(ps, g, cb, nc, nrb);
         const int stg = it % kStages;
-        mbar_expect_tx(&full[stg], (unsigned)(nrb * nc * (512 + 64) + NT * nc * 1024 + nc * 128));
-        uint8_t* sw = smem + (size_t)stg * kStageBytes;
-        const size_t t0 = tile_index(N, KC, g * kGroupBlocks, cb);  // contiguous stage range
-        bulk_g2s(sw, wt + t0 * 512, (unsigned)(nc * nrb * 512), &full[stg]);
-        bulk_g2s(sw + kStageW, st + t0 * 64, (unsigned)(nc * nrb * 64), &full[stg]);
+        mbar_expect_tx(&full[stg], (unsigned)(nc * nrb * 576 + nc * rec));
+        uint8_t* s0 = smem + (size_t)stg * kStageBytes;
+        const size_t t0 = tile_index(N, KC, g * kGroupBlocks, cb);
+        if (nrb == kGroupBlocks) {  // the stage is one contiguous range of each array
+          bulk_g2s(s0, wt + t0 * 512, (unsigned)(nc * kChunkW), &full[stg]);
+          bulk_g2s(s0 + kStageS0, st + t0 * 64, (unsigned)(nc * kChunkS), &full[stg]);
+        } else {
+          for (int u = 0; u < nc; ++u) {
+            bulk_g2s(s0 + u * kChunkW, wt + (t0 + (size_t)u * nrb) * 512, (unsigned)(nrb * 512), &full[stg]);
+            bulk_g2s(s0 + kStageS0 + u * kChunkS, st + (t0 + (size_t)u * nrb) * 64, (unsigned)(nrb * 64),
+                     &full[stg]);
+          }
+        }
       };
       auto issue_acts = [&](Pos ps, int it) {
         int g, cb, nc, nrb;
         batch_info(ps, g, cb, nc, nrb);
         const int stg = it % kStages;
-        uint8_t* sa = smem + (size_t)stg * kStageBytes + kStageW + kStageS;
-        for (int nt = 0; nt < NT; ++nt)
-          bulk_g2s(sa + nt * (2 * kChunkBatch * 512), af + ((size_t)nt * Gp + 2 * cb) * 512, (unsigned)(nc * 1024),
-                   &full[stg]);
-        bulk_g2s(sa + kStageA, corr + (size_t)(2 * cb) * 64, (unsigned)(nc * 128), &full[stg]);
+        bulk_g2s(smem + (size_t)stg * kStageBytes + kStageA0, act + (size_t)cb * rec, (unsigned)(nc * rec),
+                 &full[stg]);
       };
       Pos pro[kStages];
       int npro = 0;
@@ -161,10 +236,8 @@ __global__ void __launch_bounds__(kMmThreads)
       }
       griddep_wait();
       int issued = npro;
-      if (stop != nullptr && (__ldcg(stop) & FLAG_STOP_MASK)) {
-        for (int i = 0; i < npro; ++i) issue_acts(pro[i], i);  // complete the in-flight stages, then drain
-      } else {
-        for (int i = 0; i < npro; ++i) issue_acts(pro[i], i);
+      for (int i = 0; i < npro; ++i) issue_acts(pro[i], i);  // complete the in-flight stages
+      if (stop == nullptr || !(__ldcg(stop) & FLAG_STOP_MASK)) {
         for (int it = npro; ps.w < units && ok; ++it) {
           const int stg = it % kStages;
           ok = mbar_wait(&empty[stg], ((it / kStages) - 1) & 1);
@@ -196,7 +269,6 @@ __global__ void __launch_bounds__(kMmThreads)
     // keeps every barrier of the remaining units so that no warp is left waiting.
     for (int w = blockIdx.x; w < units; w += gridDim.x) {
       const int g = w / S, sl = w % S;
-      const int nrb = min(kGroupBlocks, n16 - g * kGroupBlocks);
       const int c0 = sl * cps, c1 = min(KC, c0 + cps);
       const int nb = (c1 - c0 + kChunkBatch - 1) / kChunkBatch;
       const int rb0 = g * kGroupBlocks + warp * kRowBlocksPerWarp;
@@ -214,72 +286,13 @@ __global__ void __launch_bounds__(kMmThreads)
           ok = false;
         }
         if (!ok) continue;
-        const uint8_t* sw = smem + (size_t)stg * kStageBytes;
-        const uint8_t* ss = sw + kStageW;
-        const uint8_t* sa = ss + kStageS;
-        const uint8_t* sc = sa + kStageA;
-        const int nc = min(kChunkBatch, c1 - (c0 + b * kChunkBatch));
-#pragma unroll
-        for (int u = 0; u < kChunkBatch; ++u) {
-          if (u >= nc) break;
-          uint32_t av[kRowBlocksPerWarp][2][4];  // A fragments per row block and group
-          float2 sg[kRowBlocksPerWarp][2];        // (row gid, row gid+8) scales per group
-#pragma unroll
-          for (int r = 0; r < kRowBlocksPerWarp; ++r) {
-            const int rl = min(warp * kRowBlocksPerWarp + r, nrb - 1);  // idle warps read a valid tile
-            const uint4 wv = reinterpret_cast<const uint4*>(sw + (u * nrb + rl) * 512)[lane];
-            const uint2 sv = reinterpret_cast<const uint2*>(ss + (u * nrb + rl) * 64)[gid];
-            sg[r][0] = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));
-            sg[r][1] = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));
-            // word x/z: row gid of groups 0/1; y/w: row gid+8
-            av[r][0][0] = wv.x & 0x0F0F0F0Fu; av[r][0][2] = (wv.x >> 4) & 0x0F0F0F0Fu;
-            av[r][0][1] = wv.y & 0x0F0F0F0Fu; av[r][0][3] = (wv.y >> 4) & 0x0F0F0F0Fu;
-            av[r][1][0] = wv.z & 0x0F0F0F0Fu; av[r][1][2] = (wv.z >> 4) & 0x0F0F0F0Fu;
-            av[r][1][1] = wv.w & 0x0F0F0F0Fu; av[r][1][3] = (wv.w >> 4) & 0x0F0F0F0Fu;
-          }
-          uint4 bf[2][NT];
-          float2 cr[2][NT];
-#pragma unroll
-          for (int gg = 0; gg < 2; ++gg)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              bf[gg][nt] = reinterpret_cast<const uint4*>(sa + nt * (2 * kChunkBatch * 512) + (2 * u + gg) * 512)[lane];
-              // negated zero-point corrections of tokens 2*tig, 2*tig+1 (see act_prep)
-              cr[gg][nt] = reinterpret_cast<const float2*>(sc + (2 * u + gg) * 64)[nt * 4 + tig];
-            }
-          // independent MMAs first: codes x lo, starting from the correction; every partial
-          // value is an integer times 2^-9 below 2^16 in magnitude, so accumulation is exact
-          float d[kRowBlocksPerWarp][2][NT][4];
-#pragma unroll
-          for (int r = 0; r < kRowBlocksPerWarp; ++r)
-#pragma unroll
-            for (int gg = 0; gg < 2; ++gg)
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                mma_e4m3(d[r][gg][nt], av[r][gg][0], av[r][gg][1], av[r][gg][2], av[r][gg][3], bf[gg][nt].z,
-                         bf[gg][nt].w, cr[gg][nt].x, cr[gg][nt].y, cr[gg][nt].x, cr[gg][nt].y);
-          // + codes x 16*hi
-#pragma unroll
-          for (int r = 0; r < kRowBlocksPerWarp; ++r)
-#pragma unroll
-            for (int gg = 0; gg < 2; ++gg)
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                mma_e4m3(d[r][gg][nt], av[r][gg][0], av[r][gg][1], av[r][gg][2], av[r][gg][3], bf[gg][nt].x,
-                         bf[gg][nt].y, d[r][gg][nt][0], d[r][gg][nt][1], d[r][gg][nt][2], d[r][gg][nt][3]);
-          // scale and accumulate, groups in ascending order
-#pragma unroll
-          for (int gg = 0; gg < 2; ++gg)
-#pragma unroll
-            for (int r = 0; r < kRowBlocksPerWarp; ++r)
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                acc[r][nt][0] = fmaf(sg[r][gg].x, d[r][gg][nt][0], acc[r][nt][0]);
-                acc[r][nt][1] = fmaf(sg[r][gg].x, d[r][gg][nt][1], acc[r][nt][1]);
-                acc[r][nt][2] = fmaf(sg[r][gg].y, d[r][gg][nt][2], acc[r][nt][2]);
-                acc[r][nt][3] = fmaf(sg[r][gg].y, d[r][gg][nt][3], acc[r][nt][3]);
-              }
-        }
+        const uint8_t* stage = smem + (size_t)stg * kStageBytes;
+        // warps past the last row block of a short row group compute on the gap (results
+        // are not stored)
+        if (c1 - (c0 + b * kChunkBatch) >= kChunkBatch)
+          mm_chunks<NT, kChunkBatch>(stage, 0, warp * kRowBlocksPerWarp, lane, acc);
+        else
+          mm_chunks<NT, 1>(stage, 0, warp * kRowBlocksPerWarp, lane, acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stg]);
       }
@@ -298,12 +311,18 @@ __global__ void __launch_bounds__(kMmThreads)
                 make_float2(acc[r][nt][2], acc[r][nt][3]);
           }
         }
-        __threadfence();
+        // The consumer barrier orders every warp's partial stores before thread 0's
+        // device-scope fence and ticket; the last ticket holder fences again before the
+        // barrier that releases the fold.
         asm volatile("bar.sync 1, %0;" ::"r"(32 * kWarpsPerCta) : "memory");
-        if (threadIdx.x == 0) s_ticket = atomicAdd(tickets + g, 1u);
+        if (threadIdx.x == 0) {
+          __threadfence();
+          const unsigned tk = atomicAdd(tickets + g, 1u);
+          if (tk == (unsigned)(S - 1)) __threadfence();
+          s_ticket = tk;
+        }
         asm volatile("bar.sync 1, %0;" ::"r"(32 * kWarpsPerCta) : "memory");
         if (s_ticket != (unsigned)(S - 1)) continue;  // not the last slice of this row group
-        __threadfence();
 #pragma unroll
         for (int r = 0; r < kRowBlocksPerWarp; ++r) {
           if (rb0 + r >= n16) continue;
@@ -354,7 +373,8 @@ __global__ void __launch_bounds__(kMmThreads)
             const int t = nt * 8 + 2 * tig + (e & 1);
             if (t >= M) continue;
             const int row = (rb0 + r) * 16 + gid + ((e & 2) ? 8 : 0);
-            const float v = acc[r][nt][e] * (512.0f * __ldg(a_s + t));
+            // acc carries the factor 2^-24 of the operand encoding
+            const float v = acc[r][nt][e] * (16777216.0f * __ldg(a_s + t));
             float* dst = y + (size_t)t * ldy + row;
             if (epi == EPI_ADD)
               *dst = *dst + v;
@@ -374,9 +394,9 @@ cudaError_t mm_configure() {
   return cudaFuncSetAttribute(k_mm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmSmem);
 }
 
-cudaError_t mm_run(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, const uint4* afrag,
-                   const float* corr, const float* a_s, int M, float* y, int ldy, int epi, float* part,
-                   unsigned* tickets, unsigned* err, const unsigned* stop, cudaStream_t stream) {
+cudaError_t mm_run(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, const uint8_t* act, const float* a_s,
+                   int M, float* y, int ldy, int epi, float* part, unsigned* tickets, unsigned* err,
+                   const unsigned* stop, cudaStream_t stream) {
   static cudaError_t configured = mm_configure();
   if (configured != cudaSuccess) return configured;
   const long long units = (long long)p.n_rg * p.S;
@@ -384,60 +404,65 @@ cudaError_t mm_run(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, 
   dim3 block(kMmThreads);
   const uint8_t* w8 = reinterpret_cast<const uint8_t*>(wt);
   const uint8_t* s8 = reinterpret_cast<const uint8_t*>(st);
-  const uint8_t* a8 = reinterpret_cast<const uint8_t*>(afrag);
-  const uint8_t* c8 = reinterpret_cast<const uint8_t*>(corr);
-  if (M <= 8)
-    return launch_pdl(k_mm<1>, grid, block, kMmSmem, stream, w8, s8, a8, c8, a_s, M, p.N, ldy, p.KC, p.cps, p.S, y,
+  if (act_tiles(M) == 1)
+    return launch_pdl(k_mm<1>, grid, block, kMmSmem, stream, w8, s8, act, a_s, M, p.N, ldy, p.KC, p.cps, p.S, y,
                       epi, part, tickets, err, stop);
-  return launch_pdl(k_mm<2>, grid, block, kMmSmem, stream, w8, s8, a8, c8, a_s, M, p.N, ldy, p.KC, p.cps, p.S, y,
-                    epi, part, tickets, err, stop);
+  return launch_pdl(k_mm<2>, grid, block, kMmSmem, stream, w8, s8, act, a_s, M, p.N, ldy, p.KC, p.cps, p.S, y, epi,
+                    part, tickets, err, stop);
 }
 
-// One warp per padded group: fragment bytes and zero-point corrections of 16 tokens.
-__global__ void k_act_prep(const int8_t* __restrict__ a_q, int M, int K, int lda, uint4* __restrict__ af,
-                           float* __restrict__ corr, unsigned* __restrict__ tickets, int n_tickets) {
+// One warp per (chunk, group, 8-token tile): lane (gid, tig) builds its f16 fragment word
+// of token 8*nt + gid and the group sums that seed the accumulators.
+__global__ void k_act_prep(const int8_t* __restrict__ a_q, int M, int K, int lda, uint8_t* __restrict__ act,
+                           unsigned* __restrict__ tickets, int n_tickets) {
   griddep_wait();
   const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
   for (int i = gtid; i < n_tickets; i += gridDim.x * blockDim.x) tickets[i] = 0u;
-  const int Gp = groups_padded(K), G = K / 32;
-  const int g = gtid >> 5;
-  if (g >= Gp) return;
+  const int NT = act_tiles(M), rec = act_rec_bytes(NT);
+  const int KC = chunks_of(K), G = K / 32;
+  const int wid = gtid >> 5;  // (c, gg, nt)
+  if (wid >= KC * 2 * NT) return;
+  const int nt = wid % NT, g = wid / NT;  // g = 2c + gg
+  const int c = g >> 1, gg = g & 1;
   const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+  const int t = nt * 8 + gid;
+  int v[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // inputs 32g + 8p + 2tig + h at 2p + h
+  if (t < M && g < G) {
+    const int8_t* src = a_q + (size_t)t * lda + 32 * g + 2 * tig;
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    const int t = nt * 8 + gid;
-    uint32_t hi0 = 0, hi1 = 0, lo0 = 0, lo1 = 0;
-    int sum = 0;
-    if (t < M && g < G) {
-      const int8_t* src = a_q + (size_t)t * lda + 32 * g + 4 * tig;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        uint32_t hb, lb;
-        const int a0 = src[b];
-        split_act(a0, hb, lb);
-        hi0 |= hb << (8 * b);
-        lo0 |= lb << (8 * b);
-        const int a1 = src[16 + b];
-        split_act(a1, hb, lb);
-        hi1 |= hb << (8 * b);
-        lo1 |= lb << (8 * b);
-        sum += a0 + a1;
-      }
+    for (int p = 0; p < 4; ++p) {
+      v[2 * p] = src[8 * p];
+      v[2 * p + 1] = src[8 * p + 1];
     }
-    af[((size_t)nt * Gp + g) * 32 + lane] = make_uint4(hi0, hi1, lo0, lo1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    if (tig == 0) corr[(size_t)g * 16 + t] = (float)sum * -0.015625f;  // -8 * sum * 2^-9
+  }
+  uint32_t h[4];
+  int sum = 0;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const float sc = (p & 1) ? 0.0625f : 1.0f;
+    const __half2 hv = __floats2half2_rn((float)v[2 * p] * sc, (float)v[2 * p + 1] * sc);
+    h[p] = *reinterpret_cast<const uint32_t*>(&hv);
+    sum += v[2 * p] + v[2 * p + 1];
+  }
+  uint8_t* rc = act + (size_t)c * rec;
+  reinterpret_cast<uint4*>(rc + (nt * 2 + gg) * 512)[lane] = make_uint4(h[0], h[1], h[2], h[3]);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  if (tig == 0) {
+    // c(t) at components (gid & 1) and 2 + (gid & 1) of the float4 of tig' = gid >> 1
+    const float cv = (float)sum * -4.76837158203125e-07f;  // -8 * 2^-24 * sum
+    float* cq = reinterpret_cast<float*>(rc + NT * 1024 + (gg * NT + nt) * 64) + (gid >> 1) * 4 + (gid & 1);
+    cq[0] = cv;
+    cq[2] = cv;
   }
 }
 
-cudaError_t act_prep_run(const int8_t* a_q, int M, int K, int lda, uint4* afrag, float* corr, unsigned* tickets,
-                         int n_tickets, cudaStream_t stream) {
-  const int Gp = groups_padded(K);
+cudaError_t act_prep_run(const int8_t* a_q, int M, int K, int lda, uint8_t* act, unsigned* tickets, int n_tickets,
+                         cudaStream_t stream) {
+  const int warps = chunks_of(K) * 2 * act_tiles(M);
   const int threads = 128;
-  const int blocks = (Gp * 32 + threads - 1) / threads;
-  return launch_pdl(k_act_prep, dim3(blocks), dim3(threads), 0, stream, a_q, M, K, lda, afrag, corr, tickets,
-                    n_tickets);
+  const int blocks = (warps * 32 + threads - 1) / threads;
+  return launch_pdl(k_act_prep, dim3(blocks), dim3(threads), 0, stream, a_q, M, K, lda, act, tickets, n_tickets);
 }
 
 }  // namespace w4a8
@@ -446,14 +471,13 @@ using namespace w4a8;
 
 namespace {
 struct MatmulWorkspace {
-  size_t off_afrag, off_corr, off_part, off_tickets, off_err, total;
+  size_t off_act, off_part, off_tickets, off_err, total;
 };
 inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 MatmulWorkspace ws_layout(const MatmulPlan& p) {
   MatmulWorkspace w;
-  w.off_afrag = 0;
-  w.off_corr = align256(w.off_afrag + afrag_uint4(p.K) * 16);
-  w.off_part = align256(w.off_corr + corr_floats(p.K) * 4);
+  w.off_act = 0;
+  w.off_part = align256(w.off_act + act_bytes(p.K));
   w.off_tickets = align256(w.off_part + p.part_floats * 4);
   w.off_err = align256(w.off_tickets + (size_t)p.n_rg * 4);
   w.total = w.off_err + 256;
@@ -484,14 +508,13 @@ W4A8_API w4a8_status w4a8_matmul(const int8_t* a_q, const float* a_s, int M, int
   if (workspace_bytes < w.total) return W4A8_ERR_CAPACITY;
   if (!aligned(a_s, 4)) return W4A8_ERR_ARG;
   char* base = static_cast<char*>(workspace);
-  uint4* af = reinterpret_cast<uint4*>(base + w.off_afrag);
-  float* corr = reinterpret_cast<float*>(base + w.off_corr);
+  uint8_t* act = reinterpret_cast<uint8_t*>(base + w.off_act);
   float* part = reinterpret_cast<float*>(base + w.off_part);
   unsigned* tickets = reinterpret_cast<unsigned*>(base + w.off_tickets);
   unsigned* err = reinterpret_cast<unsigned*>(base + w.off_err);
   cudaStream_t st = as_stream(stream);
-  W4A8_CUDA_TRY(act_prep_run(a_q, M, K, K, af, corr, tickets, p.n_rg, st));
-  W4A8_CUDA_TRY(mm_run(p, w_t, s_t, af, corr, a_s, M, y, N, EPI_STORE, part, tickets, err, nullptr, st));
+  W4A8_CUDA_TRY(act_prep_run(a_q, M, K, K, act, tickets, p.n_rg, st));
+  W4A8_CUDA_TRY(mm_run(p, w_t, s_t, act, a_s, M, y, N, EPI_STORE, part, tickets, err, nullptr, st));
   return W4A8_OK;
 }
 

@@ -28,7 +28,7 @@ enum MatmulEpilogue : int {
   EPI_ADD = 1,    // y[t][n] += value (residual stream)
 };
 
-// Launches the matmul kernel on prepared activation fragments.  part/tickets: split-K
+// Launches the matmul kernel on prepared activation records.  part/tickets: split-K
 // scratch (part_floats floats, n_rg counters that must be zero on entry; the kernel
 // leaves them zero).
 // Raises the dynamic shared-memory limit of the matmul kernels (call once per device,
@@ -38,41 +38,49 @@ cudaError_t mm_configure();
 // err: device word that receives FLAG_ERR_TIMEOUT if a bounded pipeline wait expires.
 // stop: optional device control word; when it has a FLAG_STOP_MASK bit set at kernel
 // start (after the dependency wait) the kernel does nothing.
-cudaError_t mm_run(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, const uint4* afrag,
-                   const float* corr, const float* a_s, int M, float* y, int ldy, int epi, float* part,
-                   unsigned* tickets, unsigned* err, const unsigned* stop, cudaStream_t stream);
+// act: activation records of M tokens (layout.cuh), act_bytes(K) bytes.
+cudaError_t mm_run(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, const uint8_t* act, const float* a_s,
+                   int M, float* y, int ldy, int epi, float* part, unsigned* tickets, unsigned* err,
+                   const unsigned* stop, cudaStream_t stream);
 
 // P2 layout (rows [0, N)) -> rows [row0, row0 + N) of an Ntot-row tiled matrix (quant.cu).
 cudaError_t repack_run(const uint32_t* w_p2, const uint16_t* s_p2, int N, int K, int Ntot, int row0, uint32_t* w_t,
                        uint16_t* s_t, cudaStream_t st);
 
-// Launches the fragment builder for int8 activations a_q[M][K] (row stride lda) and zeroes
+// Launches the record builder for int8 activations a_q[M][K] (row stride lda) and zeroes
 // n_tickets counters.
-cudaError_t act_prep_run(const int8_t* a_q, int M, int K, int lda, uint4* afrag, float* corr,
-                         unsigned* tickets, int n_tickets, cudaStream_t stream);
+cudaError_t act_prep_run(const int8_t* a_q, int M, int K, int lda, uint8_t* act, unsigned* tickets, int n_tickets,
+                         cudaStream_t stream);
 
-// Device helper for fused producers: writes the fragment bytes of one 4-input quad.
-// For token t (< 16) and inputs k0..k0+3 (k0 % 4 == 0) with int8 codes in `codes`
-// (byte b = input k0+b), stores the hi and lo e4m3 bytes into the fragment buffer of an
-// input dimension with Gp padded groups (layout [8-token tile][Gp][32 lanes] uint4).
-__device__ __forceinline__ void afrag_store_quad(uint4* afrag, int Gp, int t, int k0, uint32_t codes) {
-  const int g = k0 >> 5;
-  const int kin = k0 & 31;              // 0..28
-  const int tig = (kin & 15) >> 2;
-  const int upper = kin >> 4;           // 0: inputs 4tig..4tig+3, 1: inputs 16+4tig..
+// Device helpers for fused producers of the activation records (layout.cuh), for M tokens
+// (NT = act_tiles(M) tiles).
+// act_store_quad: token t (< 16), inputs k0..k0+3 (k0 % 4 == 0), int8 codes in `codes`
+// (byte b = input k0+b): writes the two f16x2 words that hold them.
+__device__ __forceinline__ void act_store_quad(uint8_t* act, int NT, int t, int k0, uint32_t codes) {
+  const int g = k0 >> 5, kin = k0 & 31;
+  const int p = kin >> 3;             // f16x2 word of the fragment (inputs 8p .. 8p+7 of the group)
+  const int tig0 = (kin & 7) >> 1;    // 0 or 2: the quad spans lanes tig0 and tig0 + 1
+  const float sc = (p & 1) ? 0.0625f : 1.0f;
   const int nt = t >> 3, gid = t & 7;
-  uint32_t hi = 0, lo = 0;
+  uint8_t* frag = act + (size_t)(g >> 1) * act_rec_bytes(NT) + (nt * 2 + (g & 1)) * 512;
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const int a = (int)(int8_t)((codes >> (8 * b)) & 0xffu);
-    uint32_t hb, lb;
-    split_act(a, hb, lb);
-    hi |= hb << (8 * b);
-    lo |= lb << (8 * b);
+  for (int j = 0; j < 2; ++j) {
+    const float a0 = (float)(int8_t)((codes >> (16 * j)) & 0xffu);
+    const float a1 = (float)(int8_t)((codes >> (16 * j + 8)) & 0xffu);
+    const __half2 hv = __floats2half2_rn(a0 * sc, a1 * sc);
+    reinterpret_cast<uint32_t*>(frag + (gid * 4 + tig0 + j) * 16)[p] = *reinterpret_cast<const uint32_t*>(&hv);
   }
-  uint32_t* dst = reinterpret_cast<uint32_t*>(afrag + ((size_t)nt * Gp + g) * 32 + gid * 4 + tig);
-  dst[upper] = hi;
-  dst[2 + upper] = lo;
+}
+// act_store_corr: the accumulator seed of token t for group g, from sum = sum of its
+// int8 codes over the group.
+__device__ __forceinline__ void act_store_corr(uint8_t* act, int NT, int t, int g, int sum) {
+  const int nt = t >> 3, tl = t & 7;
+  float* cq = reinterpret_cast<float*>(act + (size_t)(g >> 1) * act_rec_bytes(NT) + NT * 1024 +
+                                       ((g & 1) * NT + nt) * 64) +
+              (tl >> 1) * 4 + (tl & 1);
+  const float cv = (float)sum * -4.76837158203125e-07f;  // -8 * 2^-24 * sum
+  cq[0] = cv;
+  cq[2] = cv;
 }
 
 }  // namespace w4a8

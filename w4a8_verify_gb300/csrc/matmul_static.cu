@@ -1,6 +1,6 @@
-// w4a8_matmul without any allocation: the scratch (activation fragments, zero-point
-// corrections, split-K partials, slice counters and a status word) lives in one file-scope
-// device array instead of a caller-provided workspace.
+// w4a8_matmul without any allocation: the scratch (activation records, split-K partials,
+// slice counters and a status word) lives in one file-scope device array instead of a
+// caller-provided workspace.
 //
 // Why: some callers of this library cannot call cudaMalloc -- code that is already inside a
 // CUDA stream capture (an allocation is not a stream operation), hosts that hand the
@@ -50,9 +50,8 @@ W4A8_API w4a8_status w4a8_matmul_noalloc(const int8_t* a_q, const float* a_s, in
   if (M > 16 || K % 32 || N % 16) return W4A8_ERR_SHAPE;
   if (!aligned(w_t, 16) || !aligned(s_t, 16) || !aligned(a_q, 4) || !aligned(a_s, 4)) return W4A8_ERR_ARG;
   const MatmulPlan p = mm_plan(K, N);
-  // [fragments][corrections][split-K partials][n_rg slice counters, status word]
-  const size_t off_corr = align256(afrag_uint4(K) * 16);
-  const size_t off_part = align256(off_corr + corr_floats(K) * 4);
+  // [activation records][split-K partials][n_rg slice counters, status word]
+  const size_t off_part = align256(act_bytes(K));
   const size_t off_tickets = align256(off_part + p.part_floats * 4);
   const size_t total = off_tickets + ((size_t)p.n_rg + 1) * 4;
   if (total > kStaticScratchBytes) return W4A8_ERR_CAPACITY;
@@ -60,14 +59,13 @@ W4A8_API w4a8_status w4a8_matmul_noalloc(const int8_t* a_q, const float* a_s, in
   const w4a8_status st = scratch_address(&base_v);
   if (st != W4A8_OK) return st;
   char* base = static_cast<char*>(base_v);
-  uint4* af = reinterpret_cast<uint4*>(base);
-  float* corr = reinterpret_cast<float*>(base + off_corr);
+  uint8_t* act = reinterpret_cast<uint8_t*>(base);
   float* part = reinterpret_cast<float*>(base + off_part);
   unsigned* tickets = reinterpret_cast<unsigned*>(base + off_tickets);
   cudaStream_t cs = as_stream(stream);
   // the fragment pass also zeroes the slice counters and the status word that follows them:
   // the array keeps the previous call's contents, and these must start at zero
-  W4A8_CUDA_TRY(act_prep_run(a_q, M, K, K, af, corr, tickets, p.n_rg + 1, cs));
-  W4A8_CUDA_TRY(mm_run(p, w_t, s_t, af, corr, a_s, M, y, N, EPI_STORE, part, tickets, tickets + p.n_rg, nullptr, cs));
+  W4A8_CUDA_TRY(act_prep_run(a_q, M, K, K, act, tickets, p.n_rg + 1, cs));
+  W4A8_CUDA_TRY(mm_run(p, w_t, s_t, act, a_s, M, y, N, EPI_STORE, part, tickets, tickets + p.n_rg, nullptr, cs));
   return W4A8_OK;
 }

@@ -116,13 +116,12 @@ __global__ void k_repack_words(const uint32_t* __restrict__ wp2, int N, int K, i
   if (g < G) {
     out = 0;
     const uint32_t* src = wp2 + row * (K / 8);
-    for (int b = 0; b < 4; ++b) {
-      const int k_lo = 32 * g + 4 * tig + b;
-      const int k_hi = k_lo + 16;
-      const uint32_t n_lo = (src[k_lo >> 3] >> (4 * (k_lo & 7))) & 15u;
-      const uint32_t n_hi = (src[k_hi >> 3] >> (4 * (k_hi & 7))) & 15u;
-      out |= (n_lo | (n_hi << 4)) << (8 * b);
-    }
+    for (int p = 0; p < 4; ++p)
+      for (int h = 0; h < 2; ++h) {
+        const int k = 32 * g + 8 * p + 2 * tig + h;
+        const uint32_t n = (src[k >> 3] >> (4 * (k & 7))) & 15u;
+        out |= n << (4 * p + 16 * h);
+      }
   }
   const size_t t = tile_index(Ntot, KC, row0 / 16 + rb, c);
   wt[t * 128 + (i & 127)] = out;

@@ -141,22 +141,22 @@ cudaError_t forward(w4a8_session* s, int N, bool head, float* logits_out, cudaSt
   TRYC(launch_embed(b, d, N, m->emb_w, m->emb_s, st));
   for (int l = 0; l < d.n_layers; ++l) {
     TRYC(launch_rmsnorm_quant(b, d, N, st));
-    TRYC(mm_run(m->p_qkv, m->qkv_w[l], m->qkv_s[l], b.af, b.corr, b.a_s, N, b.qkv, m->qkv_rows, EPI_STORE,
+    TRYC(mm_run(m->p_qkv, m->qkv_w[l], m->qkv_s[l], b.act, b.a_s, N, b.qkv, m->qkv_rows, EPI_STORE,
                 b.mm_part, b.tickets, flags, flags, st));
     TRYC(launch_rope_kv(b, d, N, l, st));
     TRYC(launch_attention(b, d, N, l, st));
-    TRYC(mm_run(m->p_o, m->o_w[l], m->o_s[l], b.af, b.corr, b.a_s, N, b.x, d.H, EPI_ADD, b.mm_part, b.tickets,
+    TRYC(mm_run(m->p_o, m->o_w[l], m->o_s[l], b.act, b.a_s, N, b.x, d.H, EPI_ADD, b.mm_part, b.tickets,
                 flags, flags, st));
     TRYC(launch_rmsnorm_quant(b, d, N, st));
-    TRYC(mm_run(m->p_gu, m->gu_w[l], m->gu_s[l], b.af, b.corr, b.a_s, N, b.gu, 2 * d.F, EPI_STORE, b.mm_part,
+    TRYC(mm_run(m->p_gu, m->gu_w[l], m->gu_s[l], b.act, b.a_s, N, b.gu, 2 * d.F, EPI_STORE, b.mm_part,
                 b.tickets, flags, flags, st));
     TRYC(launch_swiglu_quant(b, d, N, st));
-    TRYC(mm_run(m->p_dn, m->dn_w[l], m->dn_s[l], b.af, b.corr, b.a_s, N, b.x, d.H, EPI_ADD, b.mm_part, b.tickets,
+    TRYC(mm_run(m->p_dn, m->dn_w[l], m->dn_s[l], b.act, b.a_s, N, b.x, d.H, EPI_ADD, b.mm_part, b.tickets,
                 flags, flags, st));
   }
   if (head) {
     TRYC(launch_rmsnorm_quant(b, d, N, st));
-    TRYC(mm_run(m->p_lm, m->lm_w, m->lm_s, b.af, b.corr, b.a_s, N, b.logits, d.V, EPI_STORE, b.mm_part, b.tickets,
+    TRYC(mm_run(m->p_lm, m->lm_w, m->lm_s, b.act, b.a_s, N, b.logits, d.V, EPI_STORE, b.mm_part, b.tickets,
                 flags, flags, st));
     TRYC(launch_argmax(b, d, N, st));
     if (logits_out)
@@ -302,7 +302,7 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
             A.dalloc(&b.logits, (size_t)kMaxWidth * d.V * 4) &&
             A.dalloc(&b.o_part, (size_t)b.n_chunks * kMaxWidth * d.Hq * d.D * 4) &&
             A.dalloc(&b.ml_part, (size_t)b.n_chunks * kMaxWidth * d.Hq * 8) &&
-            A.dalloc(&b.af, afrag_uint4(Kmax) * 16) && A.dalloc(&b.corr, corr_floats(Kmax) * 4) &&
+            A.dalloc(&b.act, act_bytes(Kmax)) &&
             A.dalloc(&b.a_s, kMaxWidth * 4) && A.dalloc(&b.mm_part, part * 4) && A.dalloc(&b.tickets, (size_t)tick * 4) &&
             A.dalloc(&b.kcache, kv) && A.dalloc(&b.vcache, kv) &&
             A.dalloc(&b.rope, (size_t)desc->kv_cap * (d.D / 2) * sizeof(float2)) &&
@@ -322,8 +322,7 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
   }
   // zero everything that is read before written (fragment padding groups, tickets, records)
   cudaError_t e = cudaSuccess;
-  e = e == cudaSuccess ? cudaMemset(b.af, 0, afrag_uint4(Kmax) * 16) : e;
-  e = e == cudaSuccess ? cudaMemset(b.corr, 0, corr_floats(Kmax) * 4) : e;
+  e = e == cudaSuccess ? cudaMemset(b.act, 0, act_bytes(Kmax)) : e;
   e = e == cudaSuccess ? cudaMemset(b.tickets, 0, (size_t)tick * 4) : e;
   e = e == cudaSuccess ? cudaMemset(b.argmax_tickets, 0, kMaxWidth * 4) : e;
   e = e == cudaSuccess ? cudaMemset(b.ctl, 0, sizeof(SpecCtl)) : e;
@@ -676,22 +675,22 @@ W4A8_API w4a8_status w4a8_time_matmuls(w4a8_session* s, int N, int reps, double*
   cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
   cudaError_t e3 = cudaSuccess;
   for (int l = 0; l < d.n_layers && e3 == cudaSuccess && e == cudaSuccess; ++l) {
-    e3 = mm_run(m->p_qkv, m->qkv_w[l], m->qkv_s[l], b.af, b.corr, b.a_s, N, b.qkv, m->qkv_rows, EPI_STORE, b.mm_part,
+    e3 = mm_run(m->p_qkv, m->qkv_w[l], m->qkv_s[l], b.act, b.a_s, N, b.qkv, m->qkv_rows, EPI_STORE, b.mm_part,
                 b.tickets, flags, flags, cs);
     if (e3 == cudaSuccess)
-      e3 = mm_run(m->p_o, m->o_w[l], m->o_s[l], b.af, b.corr, b.a_s, N, b.gu, d.H, EPI_STORE, b.mm_part, b.tickets,
+      e3 = mm_run(m->p_o, m->o_w[l], m->o_s[l], b.act, b.a_s, N, b.gu, d.H, EPI_STORE, b.mm_part, b.tickets,
                   flags, flags, cs);
     if (e3 == cudaSuccess)
-      e3 = mm_run(m->p_gu, m->gu_w[l], m->gu_s[l], b.af, b.corr, b.a_s, N, b.gu, 2 * d.F, EPI_STORE, b.mm_part,
+      e3 = mm_run(m->p_gu, m->gu_w[l], m->gu_s[l], b.act, b.a_s, N, b.gu, 2 * d.F, EPI_STORE, b.mm_part,
                   b.tickets, flags, flags, cs);
     if (e3 == cudaSuccess)
-      e3 = mm_run(m->p_dn, m->dn_w[l], m->dn_s[l], b.af, b.corr, b.a_s, N, b.gu, d.H, EPI_STORE, b.mm_part,
+      e3 = mm_run(m->p_dn, m->dn_w[l], m->dn_s[l], b.act, b.a_s, N, b.gu, d.H, EPI_STORE, b.mm_part,
                   b.tickets, flags, flags, cs);
     bytes += mbytes(m->p_qkv) + mbytes(m->p_o) + mbytes(m->p_gu) + mbytes(m->p_dn);
     launches += 4;
   }
   if (e3 == cudaSuccess)
-    e3 = mm_run(m->p_lm, m->lm_w, m->lm_s, b.af, b.corr, b.a_s, N, b.logits, d.V, EPI_STORE, b.mm_part, b.tickets,
+    e3 = mm_run(m->p_lm, m->lm_w, m->lm_s, b.act, b.a_s, N, b.logits, d.V, EPI_STORE, b.mm_part, b.tickets,
                 flags, flags, cs);
   bytes += mbytes(m->p_lm);
   launches += 1;
