@@ -287,6 +287,7 @@ typedef struct {
   int width_steps[17];  /* steps per width */
   uint32_t flags;       /* final control flags */
   double device_us;     /* device time from the first to the last step end */
+  int64_t kernels;      /* kernel launches of the windows run (kernel nodes of their graphs) */
 } w4a8_decode_report;
 
 /* Host, synchronous: the end-to-end call.  prompt: host int32[n_prompt]; out: host

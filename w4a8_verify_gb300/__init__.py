@@ -50,7 +50,8 @@ class DecodeOpts(_c.Structure):
 
 class DecodeReport(_c.Structure):
     _fields_ = [("n_tokens", _i32), ("n_steps", _i32), ("n_windows", _i32), ("host_syncs", _i32),
-                ("accepted_drafts", _i32), ("width_steps", _i32 * 17), ("flags", _u32), ("device_us", _dbl)]
+                ("accepted_drafts", _i32), ("width_steps", _i32 * 17), ("flags", _u32), ("device_us", _dbl),
+                ("kernels", _i64)]
 
 
 FLAG_TERMINATED, FLAG_ERR_CAPACITY, FLAG_ERR_TOKEN, FLAG_ERR_TREE, FLAG_ERR_TIMEOUT = 1, 2, 4, 8, 16

@@ -57,6 +57,13 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Kernel entry: wait for the preceding grid, then let the next kernel of the stream be
+// scheduled at once; its CTAs block in their own griddepcontrol.wait until this grid has
+// completed and its writes are visible, so only the launch latency overlaps.
+__device__ __forceinline__ void griddep_enter() {
+  griddep_wait();
+  griddep_launch();
+}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll

@@ -34,7 +34,7 @@ __device__ __forceinline__ bool stopped(const SpecCtl* ctl) { return (ctl->flags
 
 __global__ void k_embed(SpecCtl* ctl, const TreeState* __restrict__ tree, int N, const uint32_t* __restrict__ ew,
                         const uint16_t* __restrict__ es, int H, int V, int kv_cap, float* __restrict__ x) {
-  griddep_wait();
+  griddep_enter();
   if (stopped(ctl)) return;
   const int i = blockIdx.x;
   const int L = (int)ctl->committed_len;
@@ -63,7 +63,7 @@ __global__ void k_embed(SpecCtl* ctl, const TreeState* __restrict__ tree, int N,
 // per slice the sum of squares (each thread its 4 inputs in order, a warp butterfly, the
 // 4 warps in order) and max |x|.
 __global__ void k_row_stats(const SpecCtl* ctl, const float* __restrict__ x, int H, float2* __restrict__ part) {
-  griddep_wait();
+  griddep_enter();
   if (stopped(ctl)) return;
   __shared__ float s_ss[4], s_mx[4];
   const int t = blockIdx.x, sl = blockIdx.y;
@@ -94,7 +94,7 @@ template <int MODE>
 __global__ void k_quant_slices(const SpecCtl* ctl, const float* __restrict__ x, int K, int ldx,
                                const float2* __restrict__ part, int nparts, float eps, uint8_t* act, int M,
                                float* a_s) {
-  griddep_wait();
+  griddep_enter();
   if (stopped(ctl)) return;
   const int t = blockIdx.x, sl = blockIdx.y;
   float mx = 0.0f, r = 1.0f;
@@ -143,7 +143,7 @@ __global__ void k_quant_slices(const SpecCtl* ctl, const float* __restrict__ x, 
 __global__ void k_rope_kv(const SpecCtl* ctl, const TreeState* __restrict__ tree, const float* __restrict__ qkv,
                           int Hq, int Hkv, int D, const float2* __restrict__ rope, float* kc, float* vc, int kv_cap,
                           float* __restrict__ qrot, float qscale) {
-  griddep_wait();
+  griddep_enter();
   if (stopped(ctl)) return;
   const int i = blockIdx.x, h = blockIdx.y, j = threadIdx.x;
   const int L = (int)ctl->committed_len;
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(256)
     k_attn_chunk(SpecCtl* ctl, const TreeState* __restrict__ tree, int N, const float* __restrict__ qrot,
                  const float* __restrict__ kc, const float* __restrict__ vc, int kv_cap, int Hq,
                  float* __restrict__ o_part, float2* __restrict__ ml_part) {
-  griddep_wait();
+  griddep_enter();
   if (stopped(ctl)) return;
   constexpr int CH = kAttnChunk;
   constexpr int R = D / 32;
@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(256)
 __global__ void k_attn_merge(const SpecCtl* ctl, const TreeState* __restrict__ tree, const float* __restrict__ o_part,
                              const float2* __restrict__ ml_part, int Hq, int D, float* __restrict__ out,
                              float2* __restrict__ mpart) {
-  griddep_wait();
+  griddep_enter();
   if (stopped(ctl)) return;
   const int i = blockIdx.x, h = blockIdx.y, dd = threadIdx.x;
   const int L = (int)ctl->committed_len;
@@ -369,7 +369,7 @@ __global__ void k_attn_merge(const SpecCtl* ctl, const TreeState* __restrict__ t
 // grid (token, slice of kQuantSlice), 128 threads: h = silu(gate) * up written over the gate
 // half of the gate|up buffer, and the slice maximum of |h|.
 __global__ void k_swiglu(const SpecCtl* ctl, float* __restrict__ gu, int F, float2* __restrict__ part) {
-  griddep_wait();
+  griddep_enter();
   if (stopped(ctl)) return;
   __shared__ float s_mx[4];
   const int t = blockIdx.x, sl = blockIdx.y;
@@ -402,7 +402,7 @@ constexpr int kArgmaxSlice = 8192;
 // last CTA of the token to finish (ticket) reduces the slice partials.
 __global__ void k_argmax(const SpecCtl* ctl, const float* __restrict__ logits, int V, float2* __restrict__ part,
                          unsigned* __restrict__ tickets, int32_t* __restrict__ pred) {
-  griddep_wait();
+  griddep_enter();
   if (stopped(ctl)) return;
   __shared__ float sv[32];
   __shared__ int si[32];

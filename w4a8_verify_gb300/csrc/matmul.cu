@@ -169,6 +169,9 @@ __global__ void __launch_bounds__(kMmThreads)
   const int n16 = N / 16;
   const int n_rg = (n16 + kGroupBlocks - 1) / kGroupBlocks;
   const int units = n_rg * S;
+  // the next kernel may be scheduled at once: its griddepcontrol.wait still waits for this
+  // grid to complete
+  griddep_launch();
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
@@ -384,7 +387,6 @@ __global__ void __launch_bounds__(kMmThreads)
         }
       }
     }
-    griddep_launch();
   }
 }
 
@@ -415,7 +417,7 @@ cudaError_t mm_run(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, 
 // of token 8*nt + gid and the group sums that seed the accumulators.
 __global__ void k_act_prep(const int8_t* __restrict__ a_q, int M, int K, int lda, uint8_t* __restrict__ act,
                            unsigned* __restrict__ tickets, int n_tickets) {
-  griddep_wait();
+  griddep_enter();
   const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
   for (int i = gtid; i < n_tickets; i += gridDim.x * blockDim.x) tickets[i] = 0u;
   const int NT = act_tiles(M), rec = act_rec_bytes(NT);

@@ -24,7 +24,7 @@ W4A8_API const char* w4a8_status_str(int s) {
   }
 }
 
-W4A8_API int w4a8_abi_version(void) { return 1; }
+W4A8_API int w4a8_abi_version(void) { return 2; }
 
 W4A8_API w4a8_status w4a8_pack_weights(const int8_t* q, int N, int K, uint32_t* w_out) {
   if (!q || !w_out || N <= 0 || K <= 0) return W4A8_ERR_ARG;
@@ -47,7 +47,7 @@ W4A8_API w4a8_status w4a8_pack_weights(const int8_t* q, int N, int K, uint32_t* 
 // One warp per (row, group of 32): absmax (exact), fp16 scale, codes, 4 packed words.
 __global__ void k_quantize_weights(const float* __restrict__ w, int N, int K, uint32_t* __restrict__ wq,
                                    uint16_t* __restrict__ ws) {
-  griddep_wait();
+  griddep_enter();
   const int G = K / 32;
   const long long item = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (item >= (long long)N * G) return;
@@ -98,7 +98,7 @@ W4A8_API w4a8_status w4a8_weight_layout_bytes(int N, int K, size_t* words_bytes,
 // [0, N) land at rows [row0, row0 + N) of an Ntot-row tiled matrix.
 __global__ void k_repack_words(const uint32_t* __restrict__ wp2, int N, int K, int Ntot, int row0,
                                uint32_t* __restrict__ wt) {
-  griddep_wait();
+  griddep_enter();
   const long long total = (long long)tiled_words(N, K);
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= total) return;
@@ -129,7 +129,7 @@ __global__ void k_repack_words(const uint32_t* __restrict__ wp2, int N, int K, i
 
 __global__ void k_repack_scales(const uint16_t* __restrict__ sp2, int N, int K, int Ntot, int row0,
                                 uint16_t* __restrict__ st) {
-  griddep_wait();
+  griddep_enter();
   const long long total = (long long)tiled_scales(N, K);
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= total) return;
@@ -173,7 +173,7 @@ W4A8_API w4a8_status w4a8_repack_weights(const uint32_t* w_p2, const uint16_t* s
 // Per-token mode: one CTA (256 threads) per row.  absmax is exact in any order.
 __global__ void k_quantize_rows_token(const float* __restrict__ x, int K, int8_t* __restrict__ q,
                                       float* __restrict__ s) {
-  griddep_wait();
+  griddep_enter();
   __shared__ float red[8];
   const int row = blockIdx.x;
   const float* xr = x + (size_t)row * K;
@@ -196,7 +196,7 @@ __global__ void k_quantize_rows_token(const float* __restrict__ x, int K, int8_t
 // Per-32 mode: one warp per (row, block).
 __global__ void k_quantize_rows_block(const float* __restrict__ x, int M, int K, int8_t* __restrict__ q,
                                       float* __restrict__ s) {
-  griddep_wait();
+  griddep_enter();
   const int G = K / 32;
   const long long item = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (item >= (long long)M * G) return;

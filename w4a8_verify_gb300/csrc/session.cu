@@ -95,7 +95,9 @@ struct w4a8_session {
   std::deque<Flight> q;
   int next_slot = 0;
   std::map<long long, cudaGraphExec_t> graphs;
+  std::map<long long, int> graph_kernels;  // kernel nodes of each window graph
   long long host_syncs = 0;
+  long long kernels = 0;                   // kernels launched by window graphs
   ~w4a8_session() {
     for (auto& kv : graphs) cudaGraphExecDestroy(kv.second);
     for (int i = 0; i < 2; ++i)
@@ -106,8 +108,10 @@ struct w4a8_session {
 
 namespace {
 
+inline long long graph_key(int N, int W, int slot) { return ((long long)N << 32) | ((long long)W << 8) | slot; }
+
 __global__ void k_init_ctl(SpecCtl* ctl, AcceptRec* rec, const int32_t* ctx, int n, int max_new) {
-  griddep_wait();
+  griddep_enter();
   if (threadIdx.x != 0) return;
   SpecCtl c;
   c.committed_len = 0;
@@ -124,7 +128,7 @@ __global__ void k_init_ctl(SpecCtl* ctl, AcceptRec* rec, const int32_t* ctx, int
 
 // Packs the control state, the window's step statistics and emitted tokens contiguously.
 __global__ void k_window_close(const SpecCtl* ctl, const StepStats* ws, const int32_t* wt, int W, uint8_t* out) {
-  griddep_wait();
+  griddep_enter();
   const int t = threadIdx.x;
   if (t < 8) reinterpret_cast<uint32_t*>(out)[t] = reinterpret_cast<const uint32_t*>(ctl)[t];
   StepStats* so = reinterpret_cast<StepStats*>(out + kRecBytesFixed);
@@ -409,7 +413,7 @@ W4A8_API w4a8_status w4a8_spec_step(w4a8_session* s, int N, void* stream) {
 
 namespace {
 w4a8_status window_graph(w4a8_session* s, int N, int W, int slot, cudaGraphExec_t* out) {
-  const long long key = ((long long)N << 32) | ((long long)W << 8) | slot;
+  const long long key = graph_key(N, W, slot);
   auto it = s->graphs.find(key);
   if (it != s->graphs.end()) {
     *out = it->second;
@@ -431,6 +435,16 @@ w4a8_status window_graph(w4a8_session* s, int N, int W, int slot, cudaGraphExec_
     (void)cudaGetLastError();
     return W4A8_ERR_CUDA;
   }
+  size_t n_nodes = 0;
+  int n_kernels = 0;
+  if (cudaGraphGetNodes(g, nullptr, &n_nodes) == cudaSuccess && n_nodes > 0) {
+    std::vector<cudaGraphNode_t> nodes(n_nodes);
+    if (cudaGraphGetNodes(g, nodes.data(), &n_nodes) == cudaSuccess)
+      for (size_t i = 0; i < n_nodes; ++i) {
+        cudaGraphNodeType t;
+        if (cudaGraphNodeGetType(nodes[i], &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) ++n_kernels;
+      }
+  }
   cudaGraphExec_t ge = nullptr;
   e = cudaGraphInstantiate(&ge, g, 0);
   cudaGraphDestroy(g);
@@ -439,6 +453,7 @@ w4a8_status window_graph(w4a8_session* s, int N, int W, int slot, cudaGraphExec_
     return W4A8_ERR_CUDA;
   }
   s->graphs[key] = ge;
+  s->graph_kernels[key] = n_kernels;
   *out = ge;
   return W4A8_OK;
 }
@@ -454,6 +469,7 @@ W4A8_API w4a8_status spec_window(w4a8_session* s, int N, int W, void* stream) {
   cudaStream_t cs = as_stream(stream);
   W4A8_CUDA_TRY(cudaGraphLaunch(ge, cs));
   W4A8_CUDA_TRY(cudaEventRecord(s->ev[slot], cs));
+  s->kernels += s->graph_kernels[graph_key(N, W, slot)];
   s->q.push_back({slot, W, N});
   s->next_slot ^= 1;
   return W4A8_OK;
@@ -579,7 +595,7 @@ W4A8_API w4a8_status w4a8_generate(w4a8_session* s, const w4a8_decode_opts* o, i
   }
   w4a8_decode_report r;
   std::memset(&r, 0, sizeof(r));
-  const long long syncs0 = s->host_syncs;
+  const long long syncs0 = s->host_syncs, kernels0 = s->kernels;
   std::vector<w4a8_step_stats> stats((size_t)o->window);
   std::vector<int32_t> toks((size_t)o->window * kMaxWidth);
   int produced = 0;
@@ -631,6 +647,7 @@ W4A8_API w4a8_status w4a8_generate(w4a8_session* s, const w4a8_decode_opts* o, i
   r.n_tokens = produced;
   r.flags = c16.flags;
   r.host_syncs = (int)(s->host_syncs - syncs0);
+  r.kernels = s->kernels - kernels0;
   r.device_us = have_t ? (double)(uint32_t)(t_last - t_first) * 1e-3 : 0.0;
   *n_out = produced;
   if (rep) *rep = r;
@@ -723,7 +740,7 @@ W4A8_API w4a8_status w4a8_time_matmuls(w4a8_session* s, int N, int reps, double*
 
 namespace {
 __global__ void k_raise_flags(SpecCtl* ctl, uint32_t f) {
-  griddep_wait();
+  griddep_enter();
   if (threadIdx.x == 0) atomicOr(&ctl->flags, f);
 }
 }  // namespace

@@ -29,7 +29,7 @@ __device__ __forceinline__ uint32_t globaltimer_lo() {
 __global__ void k_accept(SpecCtl* ctl, const TreeState* __restrict__ tree, const int32_t* __restrict__ pred, int N,
                          AcceptRec* rec, int32_t* ctx, int ctx_cap, int kv_cap, int max_width, StepStats* wstats,
                          int32_t* wtok, int wslot, int eos) {
-  griddep_wait();
+  griddep_enter();
   const int lane = threadIdx.x;
   const uint32_t flags = ctl->flags;
   if (flags & FLAG_STOP_MASK) {
@@ -105,7 +105,7 @@ __global__ void k_accept(SpecCtl* ctl, const TreeState* __restrict__ tree, const
 // Grid (layers * kv heads); each thread owns a set of dimensions and copies path rows in
 // ascending order (path[j] >= j, so no source is overwritten before it is read).
 __global__ void k_compact(const AcceptRec* __restrict__ rec, float* kc, float* vc, int Hkv, int kv_cap, int D) {
-  griddep_wait();
+  griddep_enter();
   if (!rec->valid) return;
   const int n = rec->n_commit;
   const int L = rec->L_old;
@@ -151,7 +151,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
 __global__ void __launch_bounds__(kDraftThreads)
     k_draft(SpecCtl* ctl, const AcceptRec* __restrict__ rec, const int32_t* __restrict__ ctx, TreeState* tree,
             int force) {
-  griddep_wait();
+  griddep_enter();
   if (!force && (!rec->valid || (ctl->flags & FLAG_ERR_MASK))) return;
   extern __shared__ uint8_t s_ell[];  // match length per context position
   __shared__ int s_suf[kMaxCont];
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kDraftThreads)
 
 // Prefill: the next `len` prompt tokens ctx[L_c .. L_c+len) as a chain.
 __global__ void k_chain_tree(const SpecCtl* ctl, const int32_t* __restrict__ ctx, TreeState* tree, int len) {
-  griddep_wait();
+  griddep_enter();
   const int i = threadIdx.x;
   const int L = (int)ctl->committed_len;
   if (i < kMaxWidth) {
@@ -294,7 +294,7 @@ __global__ void k_chain_tree(const SpecCtl* ctl, const int32_t* __restrict__ ctx
 }
 
 __global__ void k_commit_chain(SpecCtl* ctl, int len) {
-  griddep_wait();
+  griddep_enter();
   if (threadIdx.x == 0 && !(ctl->flags & FLAG_ERR_MASK)) ctl->committed_len += (uint32_t)len;
 }
 
