@@ -62,7 +62,8 @@ __global__ void k_embed(SpecCtl* ctl, const TreeState* __restrict__ tree, int N,
 // Row statistics for RMSNorm, grid (token, slice of kQuantSlice inputs), 128 threads:
 // per slice the sum of squares (each thread its 4 inputs in order, a warp butterfly, the
 // 4 warps in order) and max |x|.
-__global__ void k_row_stats(const SpecCtl* ctl, const float* __restrict__ x, int H, float2* __restrict__ part) {
+__global__ void k_row_stats(const SpecCtl* ctl, float* __restrict__ x, int H, float2* __restrict__ part,
+                            const float* __restrict__ res, int res_S, const float* __restrict__ res_as) {
   griddep_enter();
   if (stopped(ctl)) return;
   __shared__ float s_ss[4], s_mx[4];
@@ -70,7 +71,14 @@ __global__ void k_row_stats(const SpecCtl* ctl, const float* __restrict__ x, int
   const int k = sl * kQuantSlice + 4 * threadIdx.x;
   float ss = 0.0f, mx = 0.0f;
   if (k < H) {
-    const float4 v = *reinterpret_cast<const float4*>(x + (size_t)t * H + k);
+    float4 v = *reinterpret_cast<const float4*>(x + (size_t)t * H + k);
+    if (res != nullptr) {  // residual update by the preceding projection (its slices folded here)
+      v.x = v.x + mm_fold(res, res_S, H, t, k, res_as);
+      v.y = v.y + mm_fold(res, res_S, H, t, k + 1, res_as);
+      v.z = v.z + mm_fold(res, res_S, H, t, k + 2, res_as);
+      v.w = v.w + mm_fold(res, res_S, H, t, k + 3, res_as);
+      *reinterpret_cast<float4*>(x + (size_t)t * H + k) = v;
+    }
     ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss); ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
     mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
   }
@@ -140,8 +148,10 @@ __global__ void k_quant_slices(const SpecCtl* ctl, const float* __restrict__ x, 
 // ------------------------------------------------------------------------- RoPE + KV
 
 // grid (node, head among Hq query + Hkv key + Hkv value heads), D/2 threads
-__global__ void k_rope_kv(const SpecCtl* ctl, const TreeState* __restrict__ tree, const float* __restrict__ qkv,
-                          int Hq, int Hkv, int D, const float2* __restrict__ rope, float* kc, float* vc, int kv_cap,
+// The projection's output rows come from its EPI_PARTIAL slices (folded here).
+__global__ void k_rope_kv(const SpecCtl* ctl, const TreeState* __restrict__ tree, const float* __restrict__ qkv_part,
+                          int qkv_S, const float* __restrict__ a_s, int Hq, int Hkv, int D,
+                          const float2* __restrict__ rope, float* kc, float* vc, int kv_cap,
                           float* __restrict__ qrot, float qscale) {
   griddep_enter();
   if (stopped(ctl)) return;
@@ -150,15 +160,16 @@ __global__ void k_rope_kv(const SpecCtl* ctl, const TreeState* __restrict__ tree
   const int pos = L + tree->depth[i];
   const int slot = L + i;
   const int half = D / 2;
-  const float* row = qkv + (size_t)i * (Hq + 2 * Hkv) * D + (size_t)h * D;
+  const int rows = (Hq + 2 * Hkv) * D;
+  const float a = mm_fold(qkv_part, qkv_S, rows, i, h * D + j, a_s);
+  const float b = mm_fold(qkv_part, qkv_S, rows, i, h * D + j + half, a_s);
   if (h >= Hq + Hkv) {  // value head: plain copy into the cache
     float* vr = vc + ((size_t)(h - Hq - Hkv) * kv_cap + slot) * D;
-    vr[j] = row[j];
-    vr[j + half] = row[j + half];
+    vr[j] = a;
+    vr[j + half] = b;
     return;
   }
   const float2 c = rope[(size_t)pos * half + j];
-  const float a = row[j], b = row[j + half];
   const float o1 = a * c.x - b * c.y;
   const float o2 = b * c.x + a * c.y;
   if (h < Hq) {
@@ -173,57 +184,148 @@ __global__ void k_rope_kv(const SpecCtl* ctl, const TreeState* __restrict__ tree
 
 // ---------------------------------------------------------------------- tree attention
 
-// Chunk pass, grid (chunk of kAttnChunk logical positions, KV head).  A warp task is (tree node,
-// GW of the G query heads of the KV head); warps take tasks round-robin (GW = G for wide trees,
-// GW = 1 when N * G <= 8 so that small trees still use several warps).  The chunk's cached K and V rows (contiguous)
-// and the tree rows are fetched with cp.async.bulk.  A warp scores the keys of its node for all
-// G query heads of the KV head at once (each key and value read serves G queries); lane j takes
-// the keys at chunk slots j and j+32.  The dot product of the key at slot j runs over the
-// dimensions starting at (j mod 32) and wrapping (conflict-free shared-memory reads); the
-// value sum of a (head, dimension) runs over positions in order.  Every order is a function of
-// the logical position only.
-template <int D, int G, int GW>
-__global__ void __launch_bounds__(256)
+constexpr int kAttnStages = 2;                      // chunks in flight (K and V entries of 64 rows each)
+constexpr int kAttnWarps = 8;                       // compute warps; one more warp issues the copies
+constexpr int kAttnThreads = 32 * (kAttnWarps + 1);
+
+// Shared-memory carve-up of the chunk kernel for head size D and at most QN queries.
+struct AttnLayout {
+  size_t stage, q, kt, vt, sp, total;
+};
+__host__ __device__ inline AttnLayout attn_layout(int D, int QN) {
+  AttnLayout a;
+  a.stage = (size_t)2 * kAttnChunk * D * 4;         // ring entry 2s: K rows, 2s + 1: V rows
+  a.q = kAttnStages * a.stage;                       // queries [q][D]
+  a.kt = a.q + (size_t)QN * D * 4;                   // tree K rows [16][D]
+  a.vt = a.kt + (size_t)kMaxWidth * D * 4;           // tree V rows
+  a.sp = a.vt + (size_t)kMaxWidth * D * 4;           // scores [q][64]
+  a.total = a.sp + (size_t)QN * kAttnChunk * 4;
+  return a;
+}
+
+// Consumer-warp barrier with an AND vote (the copy warp does not take part).
+__device__ __forceinline__ bool consumers_all(bool v) {
+  unsigned r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((unsigned)v), "r"(32 * kAttnWarps)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(32 * kAttnWarps) : "memory");
+}
+
+// Quarter dot product of the score of (query row qr, key row kr) for quarter r of a key at
+// logical position p: dimensions r*DQ + ((t + rot) mod DQ), t ascending, with the rotation
+// rot = 4 * (((p & 1) << 2 | r)) mod DQ (a function of the position; it spreads the
+// shared-memory reads of a warp over the banks).
+template <int D>
+__device__ __forceinline__ int quarter_rot(int p, int r) {
+  return (4 * (((p & 1) << 2) | r)) % (D / 4);
+}
+
+// Chunk pass, grid (split sp, KV head kh): the CTA takes chunks c = sp, sp + gridDim.x, ...
+// of kAttnChunk logical positions, streaming each chunk's cached K and V rows (contiguous)
+// through a kAttnStages-deep cp.async.bulk ring, and computes for every query of the KV
+// head (node i, head g; q = i*G + g) the chunk partial (m, l, o):
+//   scores: s = q . k as four quarter chains (quarter_rot order) added as (c0 + c1) + (c2 + c3);
+//           lane (slot j, quarter r) keeps its key quarter in registers and serves every query;
+//   m = max over the visible slots, e_j = exp(s_j - m), l = butterfly sum over the 64 slots;
+//   o[d] = sum over the visible slots j in ascending order of e_j * v_j[d] (one fmaf chain).
+// Slots below the committed length L read the cache; slots at L + e read the node's
+// ancestor at depth e (tree rows).  Every order is a function of the logical position only.
+// Warp w owns queries w, w + 8, ... (QT of them at most) for the statistics and the values.
+template <int D, int G, int QT>
+__global__ void __launch_bounds__(kAttnThreads)
     k_attn_chunk(SpecCtl* ctl, const TreeState* __restrict__ tree, int N, const float* __restrict__ qrot,
                  const float* __restrict__ kc, const float* __restrict__ vc, int kv_cap, int Hq,
                  float* __restrict__ o_part, float2* __restrict__ ml_part) {
-  griddep_enter();
-  if (stopped(ctl)) return;
   constexpr int CH = kAttnChunk;
-  constexpr int R = D / 32;
-  extern __shared__ __align__(128) float sm[];
+  constexpr int DQ = D / 4;          // quarter length
+  constexpr int DL = D / 32;         // value dimensions per lane
+  constexpr int NE = 2 * kAttnStages;  // ring entries (K or V rows of one chunk)
+  static_assert(D == 64 || D == 128, "head size");
+  // The committed length, the tree shape and the cached rows below it were written by
+  // earlier steps, so the copies of the cached rows start before the dependency wait (the
+  // kernel just before this one writes only the tree slots and the queries).
+  griddep_launch();
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_path[kMaxWidth][kMaxWidth];
   __shared__ int s_dep[kMaxWidth];
-  __shared__ uint64_t bar;
-  const int c = blockIdx.x, kh = blockIdx.y;
+  __shared__ uint64_t full[NE], empty[NE];
+  const int kh = blockIdx.y;
   const int L = (int)ctl->committed_len;
-  const int P0 = c * CH;
   int maxd = 0;
   for (int i = 0; i < N; ++i) maxd = max(maxd, tree->depth[i]);
-  if (P0 > L + maxd) return;  // uniform over the CTA
-  const int ncache = max(0, min(CH, L - P0));
-  const bool need_tree = P0 + CH > L;
-  float* Ks = sm;
-  float* Vs = Ks + CH * D;
-  float* Kt = Vs + CH * D;
-  float* Vt = Kt + kMaxWidth * D;
-  float* Qs = Vt + kMaxWidth * D;  // [node][G][D]
+  const int nch = (L + maxd) / CH + 1;
+  if ((int)blockIdx.x >= nch) return;  // uniform over the CTA
+  const int QN = N * G;
+  const AttnLayout lay = attn_layout(D, QN);
+  float* Qs = reinterpret_cast<float*>(smem + lay.q);
+  float* Kt = reinterpret_cast<float*>(smem + lay.kt);
+  float* Vt = reinterpret_cast<float*>(smem + lay.vt);
+  float* SP = reinterpret_cast<float*>(smem + lay.sp);
   const float* kb = kc + (size_t)kh * kv_cap * D;
   const float* vb = vc + (size_t)kh * kv_cap * D;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t half = lay.stage / 2;  // bytes of one ring entry
   if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
+    for (int i = 0; i < NE; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    mbar_expect_tx(&bar, (unsigned)((ncache + (need_tree ? N : 0)) * D * 4 * 2));
-    if (ncache > 0) {
-      bulk_g2s(Ks, kb + (size_t)P0 * D, (unsigned)(ncache * D * 4), &bar);
-      bulk_g2s(Vs, vb + (size_t)P0 * D, (unsigned)(ncache * D * 4), &bar);
-    }
-    if (need_tree) {
-      bulk_g2s(Kt, kb + (size_t)L * D, (unsigned)(N * D * 4), &bar);
-      bulk_g2s(Vt, vb + (size_t)L * D, (unsigned)(N * D * 4), &bar);
-    }
   }
+  __syncthreads();
+
+  if (warp == kAttnWarps) {
+    // ---------------- copy warp: entries K(c0) V(c0) K(c1) V(c1) ... ----------------
+    if (lane == 0) {
+      int n = 0;  // entries issued
+      for (int c = blockIdx.x; c < nch; c += gridDim.x) {
+        const int P0 = c * CH;
+        const int ncache = max(0, min(CH, L - P0));
+        for (int kv = 0; kv < 2; ++kv, ++n) {
+          const int e = n % NE;
+          if (n >= NE && !mbar_wait(&empty[e], ((n / NE) - 1) & 1)) {
+            atomicOr(&ctl->flags, FLAG_ERR_TIMEOUT);
+            c = nch;
+            break;
+          }
+          mbar_expect_tx(&full[e], (unsigned)(ncache * D * 4));
+          if (ncache > 0)
+            bulk_g2s(smem + (size_t)e * half, (kv ? vb : kb) + (size_t)P0 * D, (unsigned)(ncache * D * 4),
+                     &full[e]);
+        }
+      }
+      // every issued copy lands before the CTA exits
+      for (int j = max(0, n - NE); j < n; ++j)
+        if (!mbar_wait(&full[j % NE], (j / NE) & 1)) {
+          atomicOr(&ctl->flags, FLAG_ERR_TIMEOUT);
+          break;
+        }
+    }
+    return;
+  }
+
+  griddep_wait();
+  if (!consumers_all(!stopped(ctl))) {
+    // keep the ring consistent for the copy warp: consume every entry it issues
+    // (error state: nothing is computed)
+    int n = 0;
+    for (int c = blockIdx.x; c < nch; c += gridDim.x)
+      for (int kv = 0; kv < 2; ++kv, ++n) {
+        const int e = n % NE;
+        const bool got = consumers_all(mbar_wait(&full[e], (n / NE) & 1));
+        if (threadIdx.x == 0) mbar_arrive(&empty[e]);
+        if (!got) return;
+      }
+    return;
+  }
+  // ---------------- compute warps ----------------
   if (threadIdx.x < N) {
     const int i = threadIdx.x;
     const int d = tree->depth[i];
@@ -234,126 +336,222 @@ __global__ void __launch_bounds__(256)
       cur = e > 0 ? tree->parent[cur] : 0;
     }
   }
-  // queries of the CTA's nodes: the G heads of KV head kh are consecutive in qrot
-  for (int idx = threadIdx.x; idx < N * G * D / 4; idx += blockDim.x) {
-    const int i = (4 * idx) / (G * D), rem = (4 * idx) % (G * D);
-    *reinterpret_cast<float4*>(Qs + (size_t)i * G * D + rem) =
-        *reinterpret_cast<const float4*>(qrot + ((size_t)i * Hq + kh * G) * D + rem);
+  // queries of the KV head (the G heads of kh are consecutive in qrot) and the tree rows
+  // (slots L .. L+N-1, read by the chunks that reach past L)
+  for (int idx = threadIdx.x; idx < QN * D / 4; idx += 32 * kAttnWarps) {
+    const int q = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
+    const int i = q / G, g = q % G;
+    *reinterpret_cast<float4*>(Qs + (size_t)q * D + d4) =
+        *reinterpret_cast<const float4*>(qrot + ((size_t)i * Hq + kh * G + g) * D + d4);
   }
-  __syncthreads();  // barrier initialised, paths and queries in place
-  const int ok = __syncthreads_and(mbar_wait(&bar, 0) ? 1 : 0);
-  if (!ok) {  // a bounded wait expired: report and skip the chunk
-    if (threadIdx.x == 0) atomicOr(&ctl->flags, FLAG_ERR_TIMEOUT);
-    return;
+  for (int idx = threadIdx.x; idx < N * D / 4; idx += 32 * kAttnWarps) {
+    reinterpret_cast<float4*>(Kt)[idx] = reinterpret_cast<const float4*>(kb + (size_t)L * D)[idx];
+    reinterpret_cast<float4*>(Vt)[idx] = reinterpret_cast<const float4*>(vb + (size_t)L * D)[idx];
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int NS = G / GW;  // head subsets per node
-  for (int task = warp; task < N * NS; task += blockDim.x >> 5) {
-    const int i = task / NS, hs = task % NS;
-    const int pos = L + s_dep[i];
-    if (pos < P0) continue;
-    const float* q = Qs + ((size_t)i * G + hs * GW) * D;
-    const int p0 = P0 + lane, p1 = P0 + lane + 32;
-    const bool v0 = p0 <= pos, v1 = p1 <= pos;
-    const float* k0 = v0 ? (p0 < L ? Ks + lane * D : Kt + s_path[i][p0 - L] * D) : Ks;
-    const float* k1 = v1 ? (p1 < L ? Ks + (lane + 32) * D : Kt + s_path[i][p1 - L] * D) : Ks;
-    float a0[GW], a1[GW];
-#pragma unroll
-    for (int g = 0; g < GW; ++g) a0[g] = a1[g] = 0.0f;
-#pragma unroll 8
-    for (int kk = 0; kk < D; ++kk) {
-      const int k = (kk + lane) & (D - 1);
-      const float x0 = k0[k], x1 = k1[k];
-#pragma unroll
-      for (int g = 0; g < GW; ++g) {
-        const float qk = q[g * D + k];
-        a0[g] = fmaf(qk, x0, a0[g]);
-        a1[g] = fmaf(qk, x1, a1[g]);
-      }
+  consumers_sync();
+
+  int n = 0;  // ring entries consumed
+  for (int c = blockIdx.x; c < nch; c += gridDim.x, n += 2) {
+    const int eK = n % NE, eV = (n + 1) % NE;
+    if (!consumers_all(mbar_wait(&full[eK], (n / NE) & 1))) {
+      if (threadIdx.x == 0) atomicOr(&ctl->flags, FLAG_ERR_TIMEOUT);
+      break;  // a bounded wait expired: stop computing (uniform over the compute warps)
     }
-    float e0[GW], e1[GW], mg[GW], lg[GW];
-#pragma unroll
-    for (int g = 0; g < GW; ++g) {
-      const float s0 = v0 ? a0[g] : -INFINITY, s1 = v1 ? a1[g] : -INFINITY;
-      mg[g] = warp_max(fmaxf(s0, s1));
-      e0[g] = v0 ? expf(s0 - mg[g]) : 0.0f;
-      e1[g] = v1 ? expf(s1 - mg[g]) : 0.0f;
-      float l = e0[g] + e1[g];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-      lg[g] = l;
-    }
-    float o_acc[GW][R];
-#pragma unroll
-    for (int g = 0; g < GW; ++g)
-#pragma unroll
-      for (int r = 0; r < R; ++r) o_acc[g][r] = 0.0f;
-    const int last = min(CH - 1, pos - P0);
-    for (int j = 0; j <= last; ++j) {
+    const float* Ks = reinterpret_cast<const float*>(smem + (size_t)eK * half);
+    const float* Vs = reinterpret_cast<const float*>(smem + (size_t)eV * half);
+    const int P0 = c * CH;
+    const int jc = min(CH, L - P0);  // slots below jc come from the cache
+
+    // ---- scores: lane (slot j, quarter r) over all queries, four at a time
+    {
+      const int j = 8 * warp + (lane >> 2), r = lane & 3;
       const int p = P0 + j;
-      const float* vr = p < L ? Vs + j * D : Vt + s_path[i][p - L] * D;
-      float vv[R];
+      const int rot = quarter_rot<D>(p, r);
+      float kq[DQ];  // kq[t] = K[j][r*DQ + (t + rot) % DQ]
+      if (j < jc) {
 #pragma unroll
-      for (int r = 0; r < R; ++r) vv[r] = vr[lane + 32 * r];
+        for (int t = 0; t < DQ; t += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(Ks + (size_t)j * D + r * DQ + ((t + rot) % DQ));
+          kq[t] = v.x; kq[t + 1] = v.y; kq[t + 2] = v.z; kq[t + 3] = v.w;
+        }
+      }
+      for (int q0 = 0; q0 < QN; q0 += 4) {
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (j < jc) {
 #pragma unroll
-      for (int g = 0; g < GW; ++g) {
-        const float e = __shfl_sync(0xffffffffu, j < 32 ? e0[g] : e1[g], j & 31);
+          for (int t = 0; t < DQ; t += 4) {
+            const int dd = r * DQ + ((t + rot) % DQ);
 #pragma unroll
-        for (int r = 0; r < R; ++r) o_acc[g][r] = fmaf(e, vv[r], o_acc[g][r]);
+            for (int u = 0; u < 4; ++u) {
+              const float4 qv = *reinterpret_cast<const float4*>(Qs + (size_t)min(q0 + u, QN - 1) * D + dd);
+              acc[u] = fmaf(qv.x, kq[t], acc[u]);
+              acc[u] = fmaf(qv.y, kq[t + 1], acc[u]);
+              acc[u] = fmaf(qv.z, kq[t + 2], acc[u]);
+              acc[u] = fmaf(qv.w, kq[t + 3], acc[u]);
+            }
+          }
+        } else {
+          // tree slot: the key row is the ancestor of each query's node at depth p - L
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int q = min(q0 + u, QN - 1), i = q / G;
+            if (p - L > s_dep[i]) continue;
+            const float* kr = Kt + (size_t)s_path[i][p - L] * D + r * DQ;
+            const float* qr = Qs + (size_t)q * D + r * DQ;
+            float a = 0.0f;
+            for (int t = 0; t < DQ; ++t) a = fmaf(qr[(t + rot) % DQ], kr[(t + rot) % DQ], a);
+            acc[u] = a;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float sc = acc[u] + __shfl_xor_sync(0xffffffffu, acc[u], 1);
+          sc = sc + __shfl_xor_sync(0xffffffffu, sc, 2);
+          const int q = q0 + u;
+          if (r == 0 && q < QN) SP[(size_t)q * CH + j] = (p <= L + s_dep[q / G]) ? sc : -INFINITY;
+        }
       }
     }
-#pragma unroll
-    for (int g = 0; g < GW; ++g) {
-      const size_t ob = (((size_t)c * kMaxWidth + i) * Hq + kh * G + hs * GW + g);
-#pragma unroll
-      for (int r = 0; r < R; ++r) o_part[ob * D + lane + 32 * r] = o_acc[g][r];
-      if (lane == 0) ml_part[ob] = make_float2(mg[g], lg[g]);
+    consumers_sync();
+    if (threadIdx.x == 0) mbar_arrive(&empty[eK]);  // the key rows are no longer read
+    if (!consumers_all(mbar_wait(&full[eV], ((n + 1) / NE) & 1))) {
+      if (threadIdx.x == 0) atomicOr(&ctl->flags, FLAG_ERR_TIMEOUT);
+      break;
     }
+
+    // ---- statistics and values: warp w, queries w + 8u
+    {
+      float e0[QT], e1[QT], o[QT][DL];
+      int last[QT];
+      int lmin = CH, lmax = -1;
+#pragma unroll
+      for (int u = 0; u < QT; ++u) {
+        const int q = warp + kAttnWarps * u;
+        last[u] = -1;
+        e0[u] = e1[u] = 0.0f;
+#pragma unroll
+        for (int e = 0; e < DL; ++e) o[u][e] = 0.0f;
+        if (q < QN) {
+          const int i = q / G, g = q % G;
+          last[u] = min(CH - 1, L + s_dep[i] - P0);
+          if (last[u] >= 0) {
+            const float* sq = SP + (size_t)q * CH;
+            const float s0 = sq[lane], s1 = sq[lane + 32];
+            const float m = warp_max(fmaxf(s0, s1));
+            e0[u] = (s0 == -INFINITY) ? 0.0f : expf(s0 - m);
+            e1[u] = (s1 == -INFINITY) ? 0.0f : expf(s1 - m);
+            float l = e0[u] + e1[u];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+            if (lane == 0) ml_part[((size_t)c * kMaxWidth + i) * Hq + kh * G + g] = make_float2(m, l);
+            lmin = min(lmin, last[u]);
+          }
+        }
+        lmax = max(lmax, last[u]);
+      }
+      // slots every active query sees, from the cache: no per-query tests (an inactive
+      // query has e = 0 and its sums are discarded)
+      const int jall = min(min(lmin + 1, jc), lmax + 1);
+      const int d0 = lane * DL;
+      int j = 0;
+      for (; j < min(jall, 32); ++j) {
+        float v[DL];
+        if (DL == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(Vs + (size_t)j * D + d0);
+          v[0] = t.x; v[1] = t.y; v[2 % DL] = t.z; v[3 % DL] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2*>(Vs + (size_t)j * D + d0);
+          v[0] = t.x; v[1 % DL] = t.y;
+        }
+#pragma unroll
+        for (int u = 0; u < QT; ++u) {
+          const float e = __shfl_sync(0xffffffffu, e0[u], j);
+#pragma unroll
+          for (int d = 0; d < DL; ++d) o[u][d] = fmaf(e, v[d], o[u][d]);
+        }
+      }
+      for (; j < jall; ++j) {
+        float v[DL];
+        if (DL == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(Vs + (size_t)j * D + d0);
+          v[0] = t.x; v[1] = t.y; v[2 % DL] = t.z; v[3 % DL] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2*>(Vs + (size_t)j * D + d0);
+          v[0] = t.x; v[1 % DL] = t.y;
+        }
+#pragma unroll
+        for (int u = 0; u < QT; ++u) {
+          const float e = __shfl_sync(0xffffffffu, e1[u], j - 32);
+#pragma unroll
+          for (int d = 0; d < DL; ++d) o[u][d] = fmaf(e, v[d], o[u][d]);
+        }
+      }
+      // remaining slots: per query (warp-uniform tests), cache or tree rows
+      for (; j <= lmax; ++j) {
+        const int p = P0 + j;
+#pragma unroll
+        for (int u = 0; u < QT; ++u) {
+          const float e = __shfl_sync(0xffffffffu, j < 32 ? e0[u] : e1[u], j & 31);
+          if (j > last[u]) continue;
+          const int q = warp + kAttnWarps * u;
+          const float* vr = p < L ? Vs + (size_t)j * D : Vt + (size_t)s_path[q / G][p - L] * D;
+#pragma unroll
+          for (int d = 0; d < DL; ++d) o[u][d] = fmaf(e, vr[d0 + d], o[u][d]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < QT; ++u) {
+        if (last[u] < 0) continue;
+        const int q = warp + kAttnWarps * u;
+        const int i = q / G, g = q % G;
+        float* dst = o_part + (((size_t)c * kMaxWidth + i) * Hq + kh * G + g) * D + d0;
+        if (DL == 4)
+          *reinterpret_cast<float4*>(dst) = make_float4(o[u][0], o[u][1 % DL], o[u][2 % DL], o[u][3 % DL]);
+        else
+          *reinterpret_cast<float2*>(dst) = make_float2(o[u][0], o[u][1 % DL]);
+      }
+    }
+    consumers_sync();
+    if (threadIdx.x == 0) mbar_arrive(&empty[eV]);
   }
 }
 
 // Merge of the chunk partials: grid (node, query head), one thread per dimension; chunks in
-// ascending order (M = max m_c; L = sum exp(m_c - M) l_c; O = sum exp(m_c - M) o_c).
+// ascending order (M = max m_c; L = sum exp(m_c - M) l_c; O = sum exp(m_c - M) o_c).  The
+// chunk statistics are staged in shared memory once; the partial vectors are loaded 16
+// chunks at a time.
 __global__ void k_attn_merge(const SpecCtl* ctl, const TreeState* __restrict__ tree, const float* __restrict__ o_part,
                              const float2* __restrict__ ml_part, int Hq, int D, float* __restrict__ out,
                              float2* __restrict__ mpart) {
   griddep_enter();
   if (stopped(ctl)) return;
+  extern __shared__ float2 s_ml[];  // [nc]
+  __shared__ float s_mx[4];
   const int i = blockIdx.x, h = blockIdx.y, dd = threadIdx.x;
   const int L = (int)ctl->committed_len;
   const int pos = L + tree->depth[i];
   const int nc = pos / kAttnChunk + 1;
-  const size_t stride = (size_t)kMaxWidth * Hq;  // ml entries between consecutive chunks
-  const float2* ml = ml_part + (size_t)i * Hq + h;
-  const float* op = o_part + ((size_t)i * Hq + h) * D + dd;
+  const size_t stride = (size_t)kMaxWidth * Hq;  // entries between consecutive chunks
+  for (int c = dd; c < nc; c += blockDim.x) s_ml[c] = ml_part[c * stride + (size_t)i * Hq + h];
+  __syncthreads();
   float M = -INFINITY;
-  for (int c = 0; c < nc; ++c) M = fmaxf(M, ml[c * stride].x);
+  for (int c = 0; c < nc; ++c) M = fmaxf(M, s_ml[c].x);
+  const float* op = o_part + ((size_t)i * Hq + h) * D + dd;
   float Ls = 0.0f, O = 0.0f;
-  int c = 0;
-  for (; c + 8 <= nc; c += 8) {
-    float2 m8[8];
-    float o8[8];
+  for (int c = 0; c < nc; c += 16) {
+    float o16[16];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      m8[q] = ml[(c + q) * stride];
-      o8[q] = op[(size_t)(c + q) * stride * D];
-    }
+    for (int q = 0; q < 16; ++q) o16[q] = (c + q < nc) ? op[(size_t)(c + q) * stride * D] : 0.0f;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float w = expf(m8[q].x - M);
-      Ls = fmaf(w, m8[q].y, Ls);
-      O = fmaf(w, o8[q], O);
+    for (int q = 0; q < 16; ++q) {
+      if (c + q >= nc) break;
+      const float w = expf(s_ml[c + q].x - M);
+      Ls = fmaf(w, s_ml[c + q].y, Ls);
+      O = fmaf(w, o16[q], O);
     }
-  }
-  for (; c < nc; ++c) {
-    const float2 m1 = ml[c * stride];
-    const float w = expf(m1.x - M);
-    Ls = fmaf(w, m1.y, Ls);
-    O = fmaf(w, op[(size_t)c * stride * D], O);
   }
   const float res = __fdiv_rn(O, Ls);
   out[((size_t)i * Hq + h) * D + dd] = res;
-  __shared__ float s_mx[4];
   const float mx = warp_max(fabsf(res));
   if ((dd & 31) == 0) s_mx[dd >> 5] = mx;
   __syncthreads();
@@ -368,7 +566,9 @@ __global__ void k_attn_merge(const SpecCtl* ctl, const TreeState* __restrict__ t
 
 // grid (token, slice of kQuantSlice), 128 threads: h = silu(gate) * up written over the gate
 // half of the gate|up buffer, and the slice maximum of |h|.
-__global__ void k_swiglu(const SpecCtl* ctl, float* __restrict__ gu, int F, float2* __restrict__ part) {
+// gate and up rows come from the projection's EPI_PARTIAL slices (folded here).
+__global__ void k_swiglu(const SpecCtl* ctl, const float* __restrict__ gu_part, int gu_S, const float* __restrict__ a_s,
+                         float* __restrict__ gu, int F, float2* __restrict__ part) {
   griddep_enter();
   if (stopped(ctl)) return;
   __shared__ float s_mx[4];
@@ -377,8 +577,15 @@ __global__ void k_swiglu(const SpecCtl* ctl, float* __restrict__ gu, int F, floa
   float mx = 0.0f;
   if (k < F) {
     float* g = gu + (size_t)t * 2 * F + k;
-    const float4 gv = *reinterpret_cast<const float4*>(g);
-    const float4 uv = *reinterpret_cast<const float4*>(g + F);
+    float4 gv, uv;
+    gv.x = mm_fold(gu_part, gu_S, 2 * F, t, k, a_s);
+    gv.y = mm_fold(gu_part, gu_S, 2 * F, t, k + 1, a_s);
+    gv.z = mm_fold(gu_part, gu_S, 2 * F, t, k + 2, a_s);
+    gv.w = mm_fold(gu_part, gu_S, 2 * F, t, k + 3, a_s);
+    uv.x = mm_fold(gu_part, gu_S, 2 * F, t, F + k, a_s);
+    uv.y = mm_fold(gu_part, gu_S, 2 * F, t, F + k + 1, a_s);
+    uv.z = mm_fold(gu_part, gu_S, 2 * F, t, F + k + 2, a_s);
+    uv.w = mm_fold(gu_part, gu_S, 2 * F, t, F + k + 3, a_s);
     float4 h;
     h.x = __fdiv_rn(gv.x, 1.0f + expf(-gv.x)) * uv.x;
     h.y = __fdiv_rn(gv.y, 1.0f + expf(-gv.y)) * uv.y;
@@ -447,29 +654,43 @@ __global__ void k_argmax(const SpecCtl* ctl, const float* __restrict__ logits, i
 
 // ------------------------------------------------------------------------- launchers
 
-size_t attn_smem_bytes(int D, int Nq) {
-  return sizeof(float) * ((size_t)2 * kAttnChunk * D + (size_t)2 * kMaxWidth * D + (size_t)Nq * D);
-}
+size_t attn_smem_bytes(int D, int Nq) { return attn_layout(D, Nq).total; }
 
 namespace {
-template <int D, int G>
-cudaError_t attn_dispatch(bool configure, size_t smem, const DecoderBufs& b, const ModelDims& m, int N, int layer,
-                          cudaStream_t st) {
-  if (configure) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_chunk<D, G, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_attn_chunk<D, G, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  }
+// splits per KV head: about one CTA per SM (the ring holds two 64-position chunks)
+inline int attn_splits(int Hkv) { return max(1, 148 / max(1, Hkv)); }
+
+template <int D, int G, int QT>
+cudaError_t attn_launch(bool configure, size_t smem, const DecoderBufs& b, const ModelDims& m, int N, int layer,
+                        cudaStream_t st) {
+  if (configure)
+    return cudaFuncSetAttribute(k_attn_chunk<D, G, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const size_t lstride = (size_t)m.Hkv * b.kv_cap * m.D;
   const float* kc = b.kcache + layer * lstride;
   const float* vc = b.vcache + layer * lstride;
-  if (N * G <= 8)  // small trees: one warp per (node, head)
-    return launch_pdl(k_attn_chunk<D, G, 1>, dim3(b.n_chunks, m.Hkv), dim3(32 * N * G), smem, st, b.ctl,
-                      (const TreeState*)b.tree, N, (const float*)b.qrot, kc, vc, b.kv_cap, m.Hq, b.o_part,
-                      (float2*)b.ml_part);
-  return launch_pdl(k_attn_chunk<D, G, G>, dim3(b.n_chunks, m.Hkv), dim3(32 * (N < 8 ? N : 8)), smem, st, b.ctl,
-                    (const TreeState*)b.tree, N, (const float*)b.qrot, kc, vc, b.kv_cap, m.Hq, b.o_part,
+  const int splits = min(attn_splits(m.Hkv), b.n_chunks);
+  return launch_pdl(k_attn_chunk<D, G, QT>, dim3(splits, m.Hkv), dim3(kAttnThreads), attn_smem_bytes(D, N * G), st,
+                    b.ctl, (const TreeState*)b.tree, N, (const float*)b.qrot, kc, vc, b.kv_cap, m.Hq, b.o_part,
                     (float2*)b.ml_part);
+}
+// QT: queries per compute warp, the power of two >= ceil(N*G / 8) (every variant is
+// configured up front; launching picks the one for N)
+template <int D, int G>
+cudaError_t attn_dispatch(bool configure, size_t smem, const DecoderBufs& b, const ModelDims& m, int N, int layer,
+                          cudaStream_t st) {
+  constexpr int QTMAX = (kMaxWidth * G + kAttnWarps - 1) / kAttnWarps;
+  const int qt = configure ? 1 : (N * G + kAttnWarps - 1) / kAttnWarps;
+  cudaError_t e = cudaSuccess;
+  if (configure || qt <= 1) e = attn_launch<D, G, 1>(configure, smem, b, m, N, layer, st);
+  if constexpr (QTMAX > 1)
+    if (e == cudaSuccess && (configure || (qt > 1 && qt <= 2))) e = attn_launch<D, G, 2>(configure, smem, b, m, N, layer, st);
+  if constexpr (QTMAX > 2)
+    if (e == cudaSuccess && (configure || (qt > 2 && qt <= 4))) e = attn_launch<D, G, 4>(configure, smem, b, m, N, layer, st);
+  if constexpr (QTMAX > 4)
+    if (e == cudaSuccess && (configure || (qt > 4 && qt <= 8))) e = attn_launch<D, G, 8>(configure, smem, b, m, N, layer, st);
+  if constexpr (QTMAX > 8)
+    if (e == cudaSuccess && (configure || qt > 8)) e = attn_launch<D, G, 16>(configure, smem, b, m, N, layer, st);
+  return e;
 }
 template <int D>
 cudaError_t attn_dispatch_g(int G, bool configure, size_t smem, const DecoderBufs& b, const ModelDims& m, int N,
@@ -506,21 +727,22 @@ cudaError_t launch_embed(const DecoderBufs& b, const ModelDims& m, int N, const 
                     b.kv_cap, b.x);
 }
 
-cudaError_t launch_rmsnorm_quant(const DecoderBufs& b, const ModelDims& m, int N, cudaStream_t st) {
+cudaError_t launch_rmsnorm_quant(const DecoderBufs& b, const ModelDims& m, int N, const float* res, int res_S,
+                                 cudaStream_t st) {
   const int ns = (m.H + kQuantSlice - 1) / kQuantSlice;
-  cudaError_t e = launch_pdl(k_row_stats, dim3(N, ns), dim3(kQuantSlice / 4), 0, st, (const SpecCtl*)b.ctl,
-                             (const float*)b.x, m.H, b.qpart);
+  cudaError_t e = launch_pdl(k_row_stats, dim3(N, ns), dim3(kQuantSlice / 4), 0, st, (const SpecCtl*)b.ctl, b.x, m.H,
+                             b.qpart, res, res_S, (const float*)b.a_s);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_quant_slices<1>, dim3(N, ns), dim3(kQuantSlice / 4), 0, st, (const SpecCtl*)b.ctl,
                     (const float*)b.x, m.H, m.H, (const float2*)b.qpart, ns, m.eps, b.act, N, b.a_s);
 }
 
-cudaError_t launch_rope_kv(const DecoderBufs& b, const ModelDims& m, int N, int layer, cudaStream_t st) {
+cudaError_t launch_rope_kv(const DecoderBufs& b, const ModelDims& m, int N, int layer, int qkv_S, cudaStream_t st) {
   const size_t lstride = (size_t)m.Hkv * b.kv_cap * m.D;
   const float qscale = (float)(1.0 / sqrt((double)m.D));
   return launch_pdl(k_rope_kv, dim3(N, m.Hq + 2 * m.Hkv), dim3(m.D / 2), 0, st, (const SpecCtl*)b.ctl,
-                    (const TreeState*)b.tree,
-                    (const float*)b.qkv, m.Hq, m.Hkv, m.D, (const float2*)b.rope, b.kcache + layer * lstride,
+                    (const TreeState*)b.tree, (const float*)b.mm_part, qkv_S, (const float*)b.a_s, m.Hq, m.Hkv, m.D,
+                    (const float2*)b.rope, b.kcache + layer * lstride,
                     b.vcache + layer * lstride, b.kv_cap, b.qrot, qscale);
 }
 
@@ -528,7 +750,8 @@ cudaError_t launch_attention(const DecoderBufs& b, const ModelDims& m, int N, in
   const int G = m.Hq / m.Hkv;
   cudaError_t e = attn_any(m.D, G, false, attn_smem_bytes(m.D, N * G), b, m, N, layer, st);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(k_attn_merge, dim3(N, m.Hq), dim3(m.D), 0, st, (const SpecCtl*)b.ctl, (const TreeState*)b.tree,
+  e = launch_pdl(k_attn_merge, dim3(N, m.Hq), dim3(m.D), sizeof(float2) * b.n_chunks, st, (const SpecCtl*)b.ctl,
+                 (const TreeState*)b.tree,
                  (const float*)b.o_part, (const float2*)b.ml_part, m.Hq, m.D, b.qkv, b.qpart);
   if (e != cudaSuccess) return e;
   // the attention output (in the qkv buffer, [N][Hq*D]) -> int8 fragments of the O projection
@@ -538,10 +761,10 @@ cudaError_t launch_attention(const DecoderBufs& b, const ModelDims& m, int N, in
                     b.a_s);
 }
 
-cudaError_t launch_swiglu_quant(const DecoderBufs& b, const ModelDims& m, int N, cudaStream_t st) {
+cudaError_t launch_swiglu_quant(const DecoderBufs& b, const ModelDims& m, int N, int gu_S, cudaStream_t st) {
   const int ns = (m.F + kQuantSlice - 1) / kQuantSlice;
-  cudaError_t e = launch_pdl(k_swiglu, dim3(N, ns), dim3(kQuantSlice / 4), 0, st, (const SpecCtl*)b.ctl, b.gu, m.F,
-                             b.qpart);
+  cudaError_t e = launch_pdl(k_swiglu, dim3(N, ns), dim3(kQuantSlice / 4), 0, st, (const SpecCtl*)b.ctl,
+                             (const float*)b.mm_part, gu_S, (const float*)b.a_s, b.gu, m.F, b.qpart);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_quant_slices<0>, dim3(N, ns), dim3(kQuantSlice / 4), 0, st, (const SpecCtl*)b.ctl,
                     (const float*)b.gu, m.F, 2 * m.F, (const float2*)b.qpart, ns, 0.0f, b.act, N, b.a_s);

@@ -9,10 +9,15 @@ cudaError_t attn_configure(const ModelDims& m, size_t smem);
 
 cudaError_t launch_embed(const DecoderBufs& b, const ModelDims& m, int N, const uint32_t* ew, const uint16_t* es,
                          cudaStream_t st);
-cudaError_t launch_rmsnorm_quant(const DecoderBufs& b, const ModelDims& m, int N, cudaStream_t st);
-cudaError_t launch_rope_kv(const DecoderBufs& b, const ModelDims& m, int N, int layer, cudaStream_t st);
+// res: EPI_PARTIAL slices (res_S of them) of the projection whose output is added to the
+// residual stream x before the statistics, or nullptr
+cudaError_t launch_rmsnorm_quant(const DecoderBufs& b, const ModelDims& m, int N, const float* res, int res_S,
+                                 cudaStream_t st);
+// the QKV projection's output comes from its qkv_S EPI_PARTIAL slices in b.mm_part
+cudaError_t launch_rope_kv(const DecoderBufs& b, const ModelDims& m, int N, int layer, int qkv_S, cudaStream_t st);
 cudaError_t launch_attention(const DecoderBufs& b, const ModelDims& m, int N, int layer, cudaStream_t st);
-cudaError_t launch_swiglu_quant(const DecoderBufs& b, const ModelDims& m, int N, cudaStream_t st);
+// gate|up from the gu_S EPI_PARTIAL slices in b.mm_part
+cudaError_t launch_swiglu_quant(const DecoderBufs& b, const ModelDims& m, int N, int gu_S, cudaStream_t st);
 cudaError_t launch_argmax(const DecoderBufs& b, const ModelDims& m, int N, cudaStream_t st);
 
 // spec.cu

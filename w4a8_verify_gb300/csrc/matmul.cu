@@ -300,6 +300,23 @@ __global__ void __launch_bounds__(kMmThreads)
         if (lane == 0) mbar_arrive(&empty[stg]);
       }
       // ---- unit epilogue
+      if (epi == EPI_PARTIAL) {
+        if (!ok) continue;
+#pragma unroll
+        for (int r = 0; r < kRowBlocksPerWarp; ++r) {
+          if (rb0 + r >= n16) continue;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int t = nt * 8 + 2 * tig + (e & 1);
+              if (t >= M) continue;
+              const int row = (rb0 + r) * 16 + gid + ((e & 2) ? 8 : 0);
+              part[((size_t)sl * 16 + t) * N + row] = acc[r][nt][e];
+            }
+        }
+        continue;
+      }
       if (S > 1) {
 #pragma unroll
         for (int r = 0; r < kRowBlocksPerWarp; ++r) {

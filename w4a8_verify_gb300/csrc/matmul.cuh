@@ -22,10 +22,15 @@ constexpr int kRowsPerCta = 16 * kWarpsPerCta * kRowBlocksPerWarp;  // 256
 
 MatmulPlan mm_plan(int K, int N);
 
+// floats of the EPI_PARTIAL output of a plan: [S][16 tokens][N]
+inline size_t mm_partial_floats(const MatmulPlan& p) { return (size_t)p.S * 16 * p.N; }
+
 // Output handling after the fixed-order reduction: y = fold * s_a[t], then
 enum MatmulEpilogue : int {
-  EPI_STORE = 0,  // y[t][n] = value
-  EPI_ADD = 1,    // y[t][n] += value (residual stream)
+  EPI_STORE = 0,    // y[t][n] = value
+  EPI_ADD = 1,      // y[t][n] += value (residual stream)
+  EPI_PARTIAL = 2,  // part[(s * 16 + t) * N + n] = slice s's unscaled sum, t < M; y unused.  The
+                    // consumer folds the slices with mm_fold (no tickets, no fence)
 };
 
 // Launches the matmul kernel on prepared activation records.  part/tickets: split-K
@@ -42,6 +47,24 @@ cudaError_t mm_configure();
 cudaError_t mm_run(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, const uint8_t* act, const float* a_s,
                    int M, float* y, int ldy, int epi, float* part, unsigned* tickets, unsigned* err,
                    const unsigned* stop, cudaStream_t stream);
+
+// Output (t, n) of an EPI_PARTIAL matmul with S slices and N rows: the slices folded left in
+// ascending order and scaled, the same operations (and bits) as the kernel's own fold and
+// store.  Loads are issued 8 slices at a time.
+__device__ __forceinline__ float mm_fold(const float* part, int S, int N, int t, int n, const float* a_s) {
+  float f = 0.0f;
+  for (int sb = 0; sb < S; sb += 8) {
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = (sb + q < S) ? part[((size_t)(sb + q) * 16 + t) * N + n] : 0.0f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (sb + q >= S) break;
+      f = (sb + q == 0) ? v[q] : f + v[q];
+    }
+  }
+  return f * (16777216.0f * a_s[t]);
+}
 
 // P2 layout (rows [0, N)) -> rows [row0, row0 + N) of an Ntot-row tiled matrix (quant.cu).
 cudaError_t repack_run(const uint32_t* w_p2, const uint16_t* s_p2, int N, int K, int Ntot, int row0, uint32_t* w_t,

@@ -143,23 +143,29 @@ cudaError_t forward(w4a8_session* s, int N, bool head, float* logits_out, cudaSt
   const ModelDims& d = m->d;
   unsigned* flags = &b.ctl->flags;
   TRYC(launch_embed(b, d, N, m->emb_w, m->emb_s, st));
+  // The layer projections leave per-slice partial sums (EPI_PARTIAL) that the next kernel
+  // folds: RoPE/KV, the residual update before RMSNorm, SwiGLU.
+  const float* res = nullptr;
+  int res_S = 0;
   for (int l = 0; l < d.n_layers; ++l) {
-    TRYC(launch_rmsnorm_quant(b, d, N, st));
-    TRYC(mm_run(m->p_qkv, m->qkv_w[l], m->qkv_s[l], b.act, b.a_s, N, b.qkv, m->qkv_rows, EPI_STORE,
-                b.mm_part, b.tickets, flags, flags, st));
-    TRYC(launch_rope_kv(b, d, N, l, st));
+    TRYC(launch_rmsnorm_quant(b, d, N, res, res_S, st));
+    TRYC(mm_run(m->p_qkv, m->qkv_w[l], m->qkv_s[l], b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets,
+                flags, flags, st));
+    TRYC(launch_rope_kv(b, d, N, l, m->p_qkv.S, st));
     TRYC(launch_attention(b, d, N, l, st));
-    TRYC(mm_run(m->p_o, m->o_w[l], m->o_s[l], b.act, b.a_s, N, b.x, d.H, EPI_ADD, b.mm_part, b.tickets,
+    TRYC(mm_run(m->p_o, m->o_w[l], m->o_s[l], b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets, flags,
+                flags, st));
+    TRYC(launch_rmsnorm_quant(b, d, N, b.mm_part, m->p_o.S, st));
+    TRYC(mm_run(m->p_gu, m->gu_w[l], m->gu_s[l], b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets,
                 flags, flags, st));
-    TRYC(launch_rmsnorm_quant(b, d, N, st));
-    TRYC(mm_run(m->p_gu, m->gu_w[l], m->gu_s[l], b.act, b.a_s, N, b.gu, 2 * d.F, EPI_STORE, b.mm_part,
-                b.tickets, flags, flags, st));
-    TRYC(launch_swiglu_quant(b, d, N, st));
-    TRYC(mm_run(m->p_dn, m->dn_w[l], m->dn_s[l], b.act, b.a_s, N, b.x, d.H, EPI_ADD, b.mm_part, b.tickets,
+    TRYC(launch_swiglu_quant(b, d, N, m->p_gu.S, st));
+    TRYC(mm_run(m->p_dn, m->dn_w[l], m->dn_s[l], b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets,
                 flags, flags, st));
+    res = b.mm_part;
+    res_S = m->p_dn.S;
   }
   if (head) {
-    TRYC(launch_rmsnorm_quant(b, d, N, st));
+    TRYC(launch_rmsnorm_quant(b, d, N, res, res_S, st));
     TRYC(mm_run(m->p_lm, m->lm_w, m->lm_s, b.act, b.a_s, N, b.logits, d.V, EPI_STORE, b.mm_part, b.tickets,
                 flags, flags, st));
     TRYC(launch_argmax(b, d, N, st));
@@ -293,8 +299,10 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
   b.max_window = desc->max_window;
   b.eos_id = desc->eos_id;
   const int Kmax = std::max(std::max(d.H, d.F), d.Hq * d.D);
-  size_t part = std::max({m->p_qkv.part_floats, m->p_o.part_floats, m->p_gu.part_floats, m->p_dn.part_floats,
-                          m->p_lm.part_floats});
+  // split-K scratch of the head projection (EPI_STORE) and the per-slice outputs of the layer
+  // projections (EPI_PARTIAL)
+  size_t part = std::max({m->p_lm.part_floats, mm_partial_floats(m->p_qkv), mm_partial_floats(m->p_o),
+                          mm_partial_floats(m->p_gu), mm_partial_floats(m->p_dn)});
   int tick = std::max({m->p_qkv.n_rg, m->p_o.n_rg, m->p_gu.n_rg, m->p_dn.n_rg, m->p_lm.n_rg});
   const size_t kv = (size_t)d.n_layers * d.Hkv * desc->kv_cap * d.D * sizeof(float);
   Arena& A = s->arena;
@@ -692,17 +700,17 @@ W4A8_API w4a8_status w4a8_time_matmuls(w4a8_session* s, int N, int reps, double*
   cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
   cudaError_t e3 = cudaSuccess;
   for (int l = 0; l < d.n_layers && e3 == cudaSuccess && e == cudaSuccess; ++l) {
-    e3 = mm_run(m->p_qkv, m->qkv_w[l], m->qkv_s[l], b.act, b.a_s, N, b.qkv, m->qkv_rows, EPI_STORE, b.mm_part,
-                b.tickets, flags, flags, cs);
+    e3 = mm_run(m->p_qkv, m->qkv_w[l], m->qkv_s[l], b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets,
+                flags, flags, cs);
     if (e3 == cudaSuccess)
-      e3 = mm_run(m->p_o, m->o_w[l], m->o_s[l], b.act, b.a_s, N, b.gu, d.H, EPI_STORE, b.mm_part, b.tickets,
+      e3 = mm_run(m->p_o, m->o_w[l], m->o_s[l], b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets,
                   flags, flags, cs);
     if (e3 == cudaSuccess)
-      e3 = mm_run(m->p_gu, m->gu_w[l], m->gu_s[l], b.act, b.a_s, N, b.gu, 2 * d.F, EPI_STORE, b.mm_part,
-                  b.tickets, flags, flags, cs);
+      e3 = mm_run(m->p_gu, m->gu_w[l], m->gu_s[l], b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets,
+                  flags, flags, cs);
     if (e3 == cudaSuccess)
-      e3 = mm_run(m->p_dn, m->dn_w[l], m->dn_s[l], b.act, b.a_s, N, b.gu, d.H, EPI_STORE, b.mm_part,
-                  b.tickets, flags, flags, cs);
+      e3 = mm_run(m->p_dn, m->dn_w[l], m->dn_s[l], b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets,
+                  flags, flags, cs);
     bytes += mbytes(m->p_qkv) + mbytes(m->p_o) + mbytes(m->p_gu) + mbytes(m->p_dn);
     launches += 4;
   }
