@@ -280,7 +280,11 @@ def run_ours(args, rank, world):
     sess.prefill(prompt_dev, MAX_NEW)
     mm = {}
     for N in (1, 8, 16):
+        if N == 1:
+            torch.cuda.nvtx.range_push("matmul_pass")  # lets a profiler select these launches
         us, byts, nl = sess.time_matmuls(N, reps=20)
+        if N == 1:
+            torch.cuda.nvtx.range_pop()
         mm[N] = (us, byts, nl)
     us1, bytes1, nl = mm[1]
     peaks = {}

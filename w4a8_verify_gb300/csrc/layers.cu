@@ -73,10 +73,11 @@ __global__ void k_row_stats(const SpecCtl* ctl, float* __restrict__ x, int H, fl
   if (k < H) {
     float4 v = *reinterpret_cast<const float4*>(x + (size_t)t * H + k);
     if (res != nullptr) {  // residual update by the preceding projection (its slices folded here)
-      v.x = v.x + mm_fold(res, res_S, H, t, k, res_as);
-      v.y = v.y + mm_fold(res, res_S, H, t, k + 1, res_as);
-      v.z = v.z + mm_fold(res, res_S, H, t, k + 2, res_as);
-      v.w = v.w + mm_fold(res, res_S, H, t, k + 3, res_as);
+      const float4 r = mm_fold4(res, res_S, H, t, k, res_as);
+      v.x = v.x + r.x;
+      v.y = v.y + r.y;
+      v.z = v.z + r.z;
+      v.w = v.w + r.w;
       *reinterpret_cast<float4*>(x + (size_t)t * H + k) = v;
     }
     ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss); ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
@@ -161,8 +162,8 @@ __global__ void k_rope_kv(const SpecCtl* ctl, const TreeState* __restrict__ tree
   const int slot = L + i;
   const int half = D / 2;
   const int rows = (Hq + 2 * Hkv) * D;
-  const float a = mm_fold(qkv_part, qkv_S, rows, i, h * D + j, a_s);
-  const float b = mm_fold(qkv_part, qkv_S, rows, i, h * D + j + half, a_s);
+  const float2 ab = mm_fold2(qkv_part, qkv_S, rows, i, h * D + j, h * D + j + half, a_s);
+  const float a = ab.x, b = ab.y;
   if (h >= Hq + Hkv) {  // value head: plain copy into the cache
     float* vr = vc + ((size_t)(h - Hq - Hkv) * kv_cap + slot) * D;
     vr[j] = a;
@@ -577,15 +578,8 @@ __global__ void k_swiglu(const SpecCtl* ctl, const float* __restrict__ gu_part, 
   float mx = 0.0f;
   if (k < F) {
     float* g = gu + (size_t)t * 2 * F + k;
-    float4 gv, uv;
-    gv.x = mm_fold(gu_part, gu_S, 2 * F, t, k, a_s);
-    gv.y = mm_fold(gu_part, gu_S, 2 * F, t, k + 1, a_s);
-    gv.z = mm_fold(gu_part, gu_S, 2 * F, t, k + 2, a_s);
-    gv.w = mm_fold(gu_part, gu_S, 2 * F, t, k + 3, a_s);
-    uv.x = mm_fold(gu_part, gu_S, 2 * F, t, F + k, a_s);
-    uv.y = mm_fold(gu_part, gu_S, 2 * F, t, F + k + 1, a_s);
-    uv.z = mm_fold(gu_part, gu_S, 2 * F, t, F + k + 2, a_s);
-    uv.w = mm_fold(gu_part, gu_S, 2 * F, t, F + k + 3, a_s);
+    const float4 gv = mm_fold4(gu_part, gu_S, 2 * F, t, k, a_s);
+    const float4 uv = mm_fold4(gu_part, gu_S, 2 * F, t, F + k, a_s);
     float4 h;
     h.x = __fdiv_rn(gv.x, 1.0f + expf(-gv.x)) * uv.x;
     h.y = __fdiv_rn(gv.y, 1.0f + expf(-gv.y)) * uv.y;

@@ -30,7 +30,7 @@ enum MatmulEpilogue : int {
   EPI_STORE = 0,    // y[t][n] = value
   EPI_ADD = 1,      // y[t][n] += value (residual stream)
   EPI_PARTIAL = 2,  // part[(s * 16 + t) * N + n] = slice s's unscaled sum, t < M; y unused.  The
-                    // consumer folds the slices with mm_fold (no tickets, no fence)
+                    // consumer folds the slices with mm_fold4 / mm_fold2 (no tickets, no fence)
 };
 
 // Launches the matmul kernel on prepared activation records.  part/tickets: split-K
@@ -48,22 +48,50 @@ cudaError_t mm_run(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, 
                    int M, float* y, int ldy, int epi, float* part, unsigned* tickets, unsigned* err,
                    const unsigned* stop, cudaStream_t stream);
 
-// Output (t, n) of an EPI_PARTIAL matmul with S slices and N rows: the slices folded left in
-// ascending order and scaled, the same operations (and bits) as the kernel's own fold and
-// store.  Loads are issued 8 slices at a time.
-__device__ __forceinline__ float mm_fold(const float* part, int S, int N, int t, int n, const float* a_s) {
-  float f = 0.0f;
-  for (int sb = 0; sb < S; sb += 8) {
-    float v[8];
+// Four consecutive outputs (t, n .. n+3) (n % 4 == 0) of an EPI_PARTIAL matmul with S slices
+// and N rows: the slices folded left in ascending order and scaled, the same operations (and
+// bits) as the kernel's own fold and store.  Every slice's float4 is loaded before the sums
+// (up to 16 in flight).
+__device__ __forceinline__ float4 mm_fold4(const float* part, int S, int N, int t, int n, const float* a_s) {
+  float4 f = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int sb = 0; sb < S; sb += 16) {
+    float4 v[16];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = (sb + q < S) ? part[((size_t)(sb + q) * 16 + t) * N + n] : 0.0f;
+    for (int q = 0; q < 16; ++q)
+      if (sb + q < S) v[q] = *reinterpret_cast<const float4*>(part + ((size_t)(sb + q) * 16 + t) * N + n);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < 16; ++q) {
       if (sb + q >= S) break;
-      f = (sb + q == 0) ? v[q] : f + v[q];
+      if (sb + q == 0) {
+        f = v[q];
+      } else {
+        f.x = f.x + v[q].x; f.y = f.y + v[q].y; f.z = f.z + v[q].z; f.w = f.w + v[q].w;
+      }
     }
   }
-  return f * (16777216.0f * a_s[t]);
+  const float sc = 16777216.0f * a_s[t];
+  return make_float4(f.x * sc, f.y * sc, f.z * sc, f.w * sc);
+}
+// Two outputs (t, n0) and (t, n1), same fold as mm_fold4, loads of both issued together.
+__device__ __forceinline__ float2 mm_fold2(const float* part, int S, int N, int t, int n0, int n1, const float* a_s) {
+  float f0 = 0.0f, f1 = 0.0f;
+  for (int sb = 0; sb < S; sb += 16) {
+    float v0[16], v1[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      if (sb + q < S) {
+        v0[q] = part[((size_t)(sb + q) * 16 + t) * N + n0];
+        v1[q] = part[((size_t)(sb + q) * 16 + t) * N + n1];
+      }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      if (sb + q >= S) break;
+      f0 = (sb + q == 0) ? v0[q] : f0 + v0[q];
+      f1 = (sb + q == 0) ? v1[q] : f1 + v1[q];
+    }
+  }
+  const float sc = 16777216.0f * a_s[t];
+  return make_float2(f0 * sc, f1 * sc);
 }
 
 // P2 layout (rows [0, N)) -> rows [row0, row0 + N) of an Ntot-row tiled matrix (quant.cu).
