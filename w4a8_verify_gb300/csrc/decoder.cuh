@@ -73,8 +73,8 @@ struct DecoderBufs {
   float* qrot;            // [16][Hq][D]
   float* gu;              // [16][2F]
   float* logits;          // [16][V]
-  float* o_part;          // [n_chunks][16][Hq][D]
-  float* ml_part;         // [n_chunks][16][Hq][2]
+  float* o_part;          // attention split partials [split][16][Hq][D] (split < n_chunks)
+  float* ml_part;         // [split][16][Hq] (running max, sum)
   uint8_t* act;           // activation records of the next matmul (max K)
   float* a_s;             // [16] activation scales
   float* mm_part;         // split-K partials
@@ -85,6 +85,7 @@ struct DecoderBufs {
   float2* qpart;          // [16][slices] (sum of squares, max |x|) partials of the quantisation passes
   float2* argmax_part;    // [16][vocab slices] (value, index) partials
   unsigned* argmax_tickets;  // [16], zero between kernels
+  unsigned* attn_tickets;    // [Hkv], zero between kernels
   StepStats* wstats;      // [max_window] current window's statistics
   int32_t* wtok;          // [max_window][16] emitted tokens per step of the window
   int kv_cap, ctx_cap, n_chunks, max_window;

@@ -227,22 +227,29 @@ __device__ __forceinline__ int quarter_rot(int p, int r) {
   return (4 * (((p & 1) << 2) | r)) % (D / 4);
 }
 
-// Chunk pass, grid (split sp, KV head kh): the CTA takes chunks c = sp, sp + gridDim.x, ...
-// of kAttnChunk logical positions, streaming each chunk's cached K and V rows (contiguous)
-// through a kAttnStages-deep cp.async.bulk ring, and computes for every query of the KV
-// head (node i, head g; q = i*G + g) the chunk partial (m, l, o):
+// Attention pass, grid (split sp, KV head kh).  Chunks of kAttnChunk logical positions are
+// dealt to the splits in contiguous ranges of R (R and the split count depend on the cache
+// capacity and the head count only).  The CTA streams each chunk's cached K and V rows
+// (contiguous) through a ring of 2 * kAttnStages cp.async.bulk entries and keeps, for every
+// query of the KV head (node i, head g; q = i*G + g), a running (M, L, O) over its chunks in
+// ascending order:
 //   scores: s = q . k as four quarter chains (quarter_rot order) added as (c0 + c1) + (c2 + c3);
 //           lane (slot j, quarter r) keeps its key quarter in registers and serves every query;
-//   m = max over the visible slots, e_j = exp(s_j - m), l = butterfly sum over the 64 slots;
-//   o[d] = sum over the visible slots j in ascending order of e_j * v_j[d] (one fmaf chain).
+//   per chunk: m = max(M, max over visible slots), c = exp(M - m), e_j = exp(s_j - m),
+//           L = L * c + (butterfly sum of e over the 64 slots), O[d] = O[d] * c, then
+//           O[d] = fmaf(e_j, v_j[d], O[d]) over the visible slots in ascending order; M = m.
 // Slots below the committed length L read the cache; slots at L + e read the node's
-// ancestor at depth e (tree rows).  Every order is a function of the logical position only.
-// Warp w owns queries w, w + 8, ... (QT of them at most) for the statistics and the values.
-template <int D, int G, int QT>
+// ancestor at depth e (tree rows).  The last CTA of a KV head to finish (ticket) merges the
+// splits of every query in ascending order (M = max M_s, L = sum exp(M_s - M) L_s,
+// O = sum exp(M_s - M) O_s), writes O / L and the per-(node, head) maximum |O / L| that the
+// quantiser of the O projection reads (MERGE; otherwise k_attn_merge does the same merge with
+// one CTA per (node, head)).  Every order is a function of the logical position.
+template <int D, int G, int QT, bool MERGE>
 __global__ void __launch_bounds__(kAttnThreads)
-    k_attn_chunk(SpecCtl* ctl, const TreeState* __restrict__ tree, int N, const float* __restrict__ qrot,
-                 const float* __restrict__ kc, const float* __restrict__ vc, int kv_cap, int Hq,
-                 float* __restrict__ o_part, float2* __restrict__ ml_part) {
+    k_attn(SpecCtl* ctl, const TreeState* __restrict__ tree, int N, const float* __restrict__ qrot,
+           const float* __restrict__ kc, const float* __restrict__ vc, int kv_cap, int Hq, int R,
+           float* __restrict__ o_part, float2* __restrict__ ml_part, unsigned* __restrict__ tickets,
+           float* __restrict__ out, float2* __restrict__ mpart) {
   constexpr int CH = kAttnChunk;
   constexpr int DQ = D / 4;          // quarter length
   constexpr int DL = D / 32;         // value dimensions per lane
@@ -256,12 +263,15 @@ __global__ void __launch_bounds__(kAttnThreads)
   __shared__ int s_path[kMaxWidth][kMaxWidth];
   __shared__ int s_dep[kMaxWidth];
   __shared__ uint64_t full[NE], empty[NE];
+  __shared__ unsigned s_last;
   const int kh = blockIdx.y;
   const int L = (int)ctl->committed_len;
   int maxd = 0;
   for (int i = 0; i < N; ++i) maxd = max(maxd, tree->depth[i]);
   const int nch = (L + maxd) / CH + 1;
-  if ((int)blockIdx.x >= nch) return;  // uniform over the CTA
+  const int c_begin = blockIdx.x * R, c_end = min(nch, c_begin + R);
+  if (c_begin >= nch) return;  // uniform over the CTA
+  const int nsa = (nch + R - 1) / R;  // CTAs of this head that hold chunks
   const int QN = N * G;
   const AttnLayout lay = attn_layout(D, QN);
   float* Qs = reinterpret_cast<float*>(smem + lay.q);
@@ -286,14 +296,14 @@ __global__ void __launch_bounds__(kAttnThreads)
     // ---------------- copy warp: entries K(c0) V(c0) K(c1) V(c1) ... ----------------
     if (lane == 0) {
       int n = 0;  // entries issued
-      for (int c = blockIdx.x; c < nch; c += gridDim.x) {
+      for (int c = c_begin; c < c_end; ++c) {
         const int P0 = c * CH;
         const int ncache = max(0, min(CH, L - P0));
         for (int kv = 0; kv < 2; ++kv, ++n) {
           const int e = n % NE;
           if (n >= NE && !mbar_wait(&empty[e], ((n / NE) - 1) & 1)) {
             atomicOr(&ctl->flags, FLAG_ERR_TIMEOUT);
-            c = nch;
+            c = c_end;
             break;
           }
           mbar_expect_tx(&full[e], (unsigned)(ncache * D * 4));
@@ -317,7 +327,7 @@ __global__ void __launch_bounds__(kAttnThreads)
     // keep the ring consistent for the copy warp: consume every entry it issues
     // (error state: nothing is computed)
     int n = 0;
-    for (int c = blockIdx.x; c < nch; c += gridDim.x)
+    for (int c = c_begin; c < c_end; ++c)
       for (int kv = 0; kv < 2; ++kv, ++n) {
         const int e = n % NE;
         const bool got = consumers_all(mbar_wait(&full[e], (n / NE) & 1));
@@ -351,12 +361,24 @@ __global__ void __launch_bounds__(kAttnThreads)
   }
   consumers_sync();
 
+  // running state of the queries w + 8u of this warp
+  float Mr[QT], Lr[QT], Or[QT][DL];
+#pragma unroll
+  for (int u = 0; u < QT; ++u) {
+    Mr[u] = -INFINITY;
+    Lr[u] = 0.0f;
+#pragma unroll
+    for (int d = 0; d < DL; ++d) Or[u][d] = 0.0f;
+  }
+  const int d0 = lane * DL;
+  bool ok = true;
   int n = 0;  // ring entries consumed
-  for (int c = blockIdx.x; c < nch; c += gridDim.x, n += 2) {
+  for (int c = c_begin; c < c_end; ++c, n += 2) {
     const int eK = n % NE, eV = (n + 1) % NE;
     if (!consumers_all(mbar_wait(&full[eK], (n / NE) & 1))) {
       if (threadIdx.x == 0) atomicOr(&ctl->flags, FLAG_ERR_TIMEOUT);
-      break;  // a bounded wait expired: stop computing (uniform over the compute warps)
+      ok = false;  // a bounded wait expired: stop computing (uniform over the compute warps)
+      break;
     }
     const float* Ks = reinterpret_cast<const float*>(smem + (size_t)eK * half);
     const float* Vs = reinterpret_cast<const float*>(smem + (size_t)eV * half);
@@ -417,12 +439,13 @@ __global__ void __launch_bounds__(kAttnThreads)
     if (threadIdx.x == 0) mbar_arrive(&empty[eK]);  // the key rows are no longer read
     if (!consumers_all(mbar_wait(&full[eV], ((n + 1) / NE) & 1))) {
       if (threadIdx.x == 0) atomicOr(&ctl->flags, FLAG_ERR_TIMEOUT);
+      ok = false;
       break;
     }
 
-    // ---- statistics and values: warp w, queries w + 8u
+    // ---- running statistics and values: warp w, queries w + 8u
     {
-      float e0[QT], e1[QT], o[QT][DL];
+      float e0[QT], e1[QT];
       int last[QT];
       int lmin = CH, lmax = -1;
 #pragma unroll
@@ -430,61 +453,88 @@ __global__ void __launch_bounds__(kAttnThreads)
         const int q = warp + kAttnWarps * u;
         last[u] = -1;
         e0[u] = e1[u] = 0.0f;
-#pragma unroll
-        for (int e = 0; e < DL; ++e) o[u][e] = 0.0f;
         if (q < QN) {
-          const int i = q / G, g = q % G;
-          last[u] = min(CH - 1, L + s_dep[i] - P0);
+          last[u] = min(CH - 1, L + s_dep[q / G] - P0);
           if (last[u] >= 0) {
             const float* sq = SP + (size_t)q * CH;
             const float s0 = sq[lane], s1 = sq[lane + 32];
-            const float m = warp_max(fmaxf(s0, s1));
+            const float m = fmaxf(Mr[u], warp_max(fmaxf(s0, s1)));
+            const float cs = (Mr[u] == -INFINITY) ? 0.0f : expf(Mr[u] - m);
             e0[u] = (s0 == -INFINITY) ? 0.0f : expf(s0 - m);
             e1[u] = (s1 == -INFINITY) ? 0.0f : expf(s1 - m);
             float l = e0[u] + e1[u];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-            if (lane == 0) ml_part[((size_t)c * kMaxWidth + i) * Hq + kh * G + g] = make_float2(m, l);
+            Lr[u] = fmaf(Lr[u], cs, l);
+            Mr[u] = m;
+#pragma unroll
+            for (int d = 0; d < DL; ++d) Or[u][d] = Or[u][d] * cs;
             lmin = min(lmin, last[u]);
           }
         }
         lmax = max(lmax, last[u]);
       }
       // slots every active query sees, from the cache: no per-query tests (an inactive
-      // query has e = 0 and its sums are discarded)
+      // query has e = 0 and its state is not stored); four slots per step
       const int jall = min(min(lmin + 1, jc), lmax + 1);
-      const int d0 = lane * DL;
       int j = 0;
-      for (; j < min(jall, 32); ++j) {
-        float v[DL];
+      auto vrow = [&](int jj, float (&v)[DL]) {
         if (DL == 4) {
-          const float4 t = *reinterpret_cast<const float4*>(Vs + (size_t)j * D + d0);
-          v[0] = t.x; v[1] = t.y; v[2 % DL] = t.z; v[3 % DL] = t.w;
+          const float4 t = *reinterpret_cast<const float4*>(Vs + (size_t)jj * D + d0);
+          v[0] = t.x; v[1 % DL] = t.y; v[2 % DL] = t.z; v[3 % DL] = t.w;
         } else {
-          const float2 t = *reinterpret_cast<const float2*>(Vs + (size_t)j * D + d0);
+          const float2 t = *reinterpret_cast<const float2*>(Vs + (size_t)jj * D + d0);
           v[0] = t.x; v[1 % DL] = t.y;
         }
+      };
+      for (; j + 4 <= min(jall, 32); j += 4) {
+        float v[4][DL];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) vrow(j + k, v[k]);
+#pragma unroll
+        for (int u = 0; u < QT; ++u) {
+          float e[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) e[k] = __shfl_sync(0xffffffffu, e0[u], j + k);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int d = 0; d < DL; ++d) Or[u][d] = fmaf(e[k], v[k][d], Or[u][d]);
+        }
+      }
+      for (; j < min(jall, 32); ++j) {
+        float v[DL];
+        vrow(j, v);
 #pragma unroll
         for (int u = 0; u < QT; ++u) {
           const float e = __shfl_sync(0xffffffffu, e0[u], j);
 #pragma unroll
-          for (int d = 0; d < DL; ++d) o[u][d] = fmaf(e, v[d], o[u][d]);
+          for (int d = 0; d < DL; ++d) Or[u][d] = fmaf(e, v[d], Or[u][d]);
+        }
+      }
+      for (; j + 4 <= jall; j += 4) {
+        float v[4][DL];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) vrow(j + k, v[k]);
+#pragma unroll
+        for (int u = 0; u < QT; ++u) {
+          float e[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) e[k] = __shfl_sync(0xffffffffu, e1[u], j + k - 32);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int d = 0; d < DL; ++d) Or[u][d] = fmaf(e[k], v[k][d], Or[u][d]);
         }
       }
       for (; j < jall; ++j) {
         float v[DL];
-        if (DL == 4) {
-          const float4 t = *reinterpret_cast<const float4*>(Vs + (size_t)j * D + d0);
-          v[0] = t.x; v[1] = t.y; v[2 % DL] = t.z; v[3 % DL] = t.w;
-        } else {
-          const float2 t = *reinterpret_cast<const float2*>(Vs + (size_t)j * D + d0);
-          v[0] = t.x; v[1 % DL] = t.y;
-        }
+        vrow(j, v);
 #pragma unroll
         for (int u = 0; u < QT; ++u) {
           const float e = __shfl_sync(0xffffffffu, e1[u], j - 32);
 #pragma unroll
-          for (int d = 0; d < DL; ++d) o[u][d] = fmaf(e, v[d], o[u][d]);
+          for (int d = 0; d < DL; ++d) Or[u][d] = fmaf(e, v[d], Or[u][d]);
         }
       }
       // remaining slots: per query (warp-uniform tests), cache or tree rows
@@ -497,69 +547,129 @@ __global__ void __launch_bounds__(kAttnThreads)
           const int q = warp + kAttnWarps * u;
           const float* vr = p < L ? Vs + (size_t)j * D : Vt + (size_t)s_path[q / G][p - L] * D;
 #pragma unroll
-          for (int d = 0; d < DL; ++d) o[u][d] = fmaf(e, vr[d0 + d], o[u][d]);
+          for (int d = 0; d < DL; ++d) Or[u][d] = fmaf(e, vr[d0 + d], Or[u][d]);
         }
-      }
-#pragma unroll
-      for (int u = 0; u < QT; ++u) {
-        if (last[u] < 0) continue;
-        const int q = warp + kAttnWarps * u;
-        const int i = q / G, g = q % G;
-        float* dst = o_part + (((size_t)c * kMaxWidth + i) * Hq + kh * G + g) * D + d0;
-        if (DL == 4)
-          *reinterpret_cast<float4*>(dst) = make_float4(o[u][0], o[u][1 % DL], o[u][2 % DL], o[u][3 % DL]);
-        else
-          *reinterpret_cast<float2*>(dst) = make_float2(o[u][0], o[u][1 % DL]);
       }
     }
     consumers_sync();
     if (threadIdx.x == 0) mbar_arrive(&empty[eV]);
   }
+
+  // ---- this split's partial, then the merge by the last split of the head
+  if (ok) {
+#pragma unroll
+    for (int u = 0; u < QT; ++u) {
+      const int q = warp + kAttnWarps * u;
+      if (q >= QN || L + s_dep[q / G] < c_begin * CH) continue;
+      const int i = q / G, g = q % G;
+      const size_t ob = ((size_t)blockIdx.x * kMaxWidth + i) * Hq + kh * G + g;
+      float* dst = o_part + ob * D + d0;
+      if (DL == 4)
+        *reinterpret_cast<float4*>(dst) = make_float4(Or[u][0], Or[u][1 % DL], Or[u][2 % DL], Or[u][3 % DL]);
+      else
+        *reinterpret_cast<float2*>(dst) = make_float2(Or[u][0], Or[u][1 % DL]);
+      if (lane == 0) ml_part[ob] = make_float2(Mr[u], Lr[u]);
+    }
+  }
+  if (!MERGE) return;
+  consumers_sync();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned t = atomicAdd(tickets + kh, 1u);
+    const unsigned last = (t == (unsigned)(nsa - 1)) ? 1u : 0u;
+    if (last) {
+      __threadfence();
+      tickets[kh] = 0u;
+    }
+    s_last = last;
+  }
+  consumers_sync();
+  if (!s_last) return;
+  for (int q = warp; q < QN; q += kAttnWarps) {
+    const int i = q / G, g = q % G;
+    const int smax = ((L + s_dep[i]) / CH) / R;  // splits that saw this node
+    const size_t hb = (size_t)i * Hq + kh * G + g;
+    const size_t sstride = (size_t)kMaxWidth * Hq;
+    float M = -INFINITY;
+    for (int s2 = lane; s2 <= smax; s2 += 32) M = fmaxf(M, __ldcg(&ml_part[s2 * sstride + hb].x));
+    M = warp_max(M);
+    float Ls = 0.0f, O[DL];
+#pragma unroll
+    for (int d = 0; d < DL; ++d) O[d] = 0.0f;
+    for (int sb = 0; sb <= smax; sb += 8) {
+      float2 ml[8];
+      float ov[8][DL];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (sb + k > smax) break;
+        ml[k] = __ldcg(&ml_part[(sb + k) * sstride + hb]);
+        const float* src = o_part + ((sb + k) * sstride + hb) * D + d0;
+#pragma unroll
+        for (int d = 0; d < DL; ++d) ov[k][d] = __ldcg(src + d);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (sb + k > smax) break;
+        const float w = expf(ml[k].x - M);
+        Ls = fmaf(w, ml[k].y, Ls);
+#pragma unroll
+        for (int d = 0; d < DL; ++d) O[d] = fmaf(w, ov[k][d], O[d]);
+      }
+    }
+    float mx = 0.0f;
+#pragma unroll
+    for (int d = 0; d < DL; ++d) {
+      const float res = __fdiv_rn(O[d], Ls);
+      out[hb * D + d0 + d] = res;
+      mx = fmaxf(mx, fabsf(res));
+    }
+    mx = warp_max(mx);
+    if (lane == 0) mpart[hb] = make_float2(0.0f, mx);
+  }
 }
 
-// Merge of the chunk partials: grid (node, query head), one thread per dimension; chunks in
-// ascending order (M = max m_c; L = sum exp(m_c - M) l_c; O = sum exp(m_c - M) o_c).  The
-// chunk statistics are staged in shared memory once; the partial vectors are loaded 16
-// chunks at a time.
+// Merge of the split partials for wide trees: grid (node, query head), one thread per
+// dimension; the same order and operations as the in-kernel merge of k_attn.
 __global__ void k_attn_merge(const SpecCtl* ctl, const TreeState* __restrict__ tree, const float* __restrict__ o_part,
-                             const float2* __restrict__ ml_part, int Hq, int D, float* __restrict__ out,
+                             const float2* __restrict__ ml_part, int Hq, int D, int R, float* __restrict__ out,
                              float2* __restrict__ mpart) {
   griddep_enter();
   if (stopped(ctl)) return;
-  extern __shared__ float2 s_ml[];  // [nc]
   __shared__ float s_mx[4];
   const int i = blockIdx.x, h = blockIdx.y, dd = threadIdx.x;
   const int L = (int)ctl->committed_len;
-  const int pos = L + tree->depth[i];
-  const int nc = pos / kAttnChunk + 1;
-  const size_t stride = (size_t)kMaxWidth * Hq;  // entries between consecutive chunks
-  for (int c = dd; c < nc; c += blockDim.x) s_ml[c] = ml_part[c * stride + (size_t)i * Hq + h];
-  __syncthreads();
+  const int smax = ((L + tree->depth[i]) / kAttnChunk) / R;
+  const size_t hb = (size_t)i * Hq + h;
+  const size_t sstride = (size_t)kMaxWidth * Hq;
   float M = -INFINITY;
-  for (int c = 0; c < nc; ++c) M = fmaxf(M, s_ml[c].x);
-  const float* op = o_part + ((size_t)i * Hq + h) * D + dd;
+  for (int s2 = 0; s2 <= smax; ++s2) M = fmaxf(M, ml_part[s2 * sstride + hb].x);
   float Ls = 0.0f, O = 0.0f;
-  for (int c = 0; c < nc; c += 16) {
-    float o16[16];
+  for (int sb = 0; sb <= smax; sb += 8) {
+    float2 ml[8];
+    float ov[8];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) o16[q] = (c + q < nc) ? op[(size_t)(c + q) * stride * D] : 0.0f;
+    for (int k = 0; k < 8; ++k) {
+      if (sb + k > smax) break;
+      ml[k] = ml_part[(sb + k) * sstride + hb];
+      ov[k] = o_part[((sb + k) * sstride + hb) * D + dd];
+    }
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      if (c + q >= nc) break;
-      const float w = expf(s_ml[c + q].x - M);
-      Ls = fmaf(w, s_ml[c + q].y, Ls);
-      O = fmaf(w, o16[q], O);
+    for (int k = 0; k < 8; ++k) {
+      if (sb + k > smax) break;
+      const float w = expf(ml[k].x - M);
+      Ls = fmaf(w, ml[k].y, Ls);
+      O = fmaf(w, ov[k], O);
     }
   }
   const float res = __fdiv_rn(O, Ls);
-  out[((size_t)i * Hq + h) * D + dd] = res;
+  out[hb * D + dd] = res;
   const float mx = warp_max(fabsf(res));
   if ((dd & 31) == 0) s_mx[dd >> 5] = mx;
   __syncthreads();
   if (dd == 0) {
     float m = s_mx[0];
     for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, s_mx[w]);
-    mpart[(size_t)i * Hq + h] = make_float2(0.0f, m);
+    mpart[hb] = make_float2(0.0f, m);
   }
 }
 
@@ -654,18 +764,27 @@ namespace {
 // splits per KV head: about one CTA per SM (the ring holds two 64-position chunks)
 inline int attn_splits(int Hkv) { return max(1, 148 / max(1, Hkv)); }
 
+// attn_merge_inside(QT): the last split CTA merges small trees itself; wide trees (more than
+// two queries per warp) merge in k_attn_merge, one CTA per (node, head)
+constexpr bool attn_merge_inside(int QT) { return QT <= 2; }
+
 template <int D, int G, int QT>
 cudaError_t attn_launch(bool configure, size_t smem, const DecoderBufs& b, const ModelDims& m, int N, int layer,
                         cudaStream_t st) {
+  constexpr bool MERGE = attn_merge_inside(QT);
   if (configure)
-    return cudaFuncSetAttribute(k_attn_chunk<D, G, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    return cudaFuncSetAttribute(k_attn<D, G, QT, MERGE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const size_t lstride = (size_t)m.Hkv * b.kv_cap * m.D;
   const float* kc = b.kcache + layer * lstride;
   const float* vc = b.vcache + layer * lstride;
   const int splits = min(attn_splits(m.Hkv), b.n_chunks);
-  return launch_pdl(k_attn_chunk<D, G, QT>, dim3(splits, m.Hkv), dim3(kAttnThreads), attn_smem_bytes(D, N * G), st,
-                    b.ctl, (const TreeState*)b.tree, N, (const float*)b.qrot, kc, vc, b.kv_cap, m.Hq, b.o_part,
-                    (float2*)b.ml_part);
+  const int R = (b.n_chunks + splits - 1) / splits;  // chunks per split (fixed per session)
+  cudaError_t e = launch_pdl(k_attn<D, G, QT, MERGE>, dim3(splits, m.Hkv), dim3(kAttnThreads),
+                             attn_smem_bytes(D, N * G), st, b.ctl, (const TreeState*)b.tree, N, (const float*)b.qrot,
+                             kc, vc, b.kv_cap, m.Hq, R, b.o_part, (float2*)b.ml_part, b.attn_tickets, b.qkv, b.qpart);
+  if (e != cudaSuccess || MERGE) return e;
+  return launch_pdl(k_attn_merge, dim3(N, m.Hq), dim3(m.D), 0, st, (const SpecCtl*)b.ctl, (const TreeState*)b.tree,
+                    (const float*)b.o_part, (const float2*)b.ml_part, m.Hq, m.D, R, b.qkv, b.qpart);
 }
 // QT: queries per compute warp, the power of two >= ceil(N*G / 8) (every variant is
 // configured up front; launching picks the one for N)
@@ -743,10 +862,6 @@ cudaError_t launch_rope_kv(const DecoderBufs& b, const ModelDims& m, int N, int 
 cudaError_t launch_attention(const DecoderBufs& b, const ModelDims& m, int N, int layer, cudaStream_t st) {
   const int G = m.Hq / m.Hkv;
   cudaError_t e = attn_any(m.D, G, false, attn_smem_bytes(m.D, N * G), b, m, N, layer, st);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(k_attn_merge, dim3(N, m.Hq), dim3(m.D), sizeof(float2) * b.n_chunks, st, (const SpecCtl*)b.ctl,
-                 (const TreeState*)b.tree,
-                 (const float*)b.o_part, (const float2*)b.ml_part, m.Hq, m.D, b.qkv, b.qpart);
   if (e != cudaSuccess) return e;
   // the attention output (in the qkv buffer, [N][Hq*D]) -> int8 fragments of the O projection
   const int QD = m.Hq * m.D;

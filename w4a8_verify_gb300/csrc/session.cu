@@ -320,7 +320,7 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
             A.dalloc(&b.rope, (size_t)desc->kv_cap * (d.D / 2) * sizeof(float2)) &&
             A.dalloc(&b.qpart, (size_t)kMaxWidth * (std::max({d.H, d.F, d.Hq * d.D}) / 512 + d.Hq + 2) * sizeof(float2)) &&
             A.dalloc(&b.argmax_part, (size_t)kMaxWidth * ((d.V + 8191) / 8192) * sizeof(float2)) &&
-            A.dalloc(&b.argmax_tickets, kMaxWidth * 4) &&
+            A.dalloc(&b.argmax_tickets, kMaxWidth * 4) && A.dalloc(&b.attn_tickets, (size_t)d.Hkv * 4) &&
             A.dalloc(&b.wstats, (size_t)desc->max_window * sizeof(StepStats)) &&
             A.dalloc(&b.wtok, (size_t)desc->max_window * kMaxWidth * 4) &&
             A.dalloc(&s->dev_rec, kRecBytesFixed + (size_t)desc->max_window * kRecStepBytes) &&
@@ -337,6 +337,7 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
   e = e == cudaSuccess ? cudaMemset(b.act, 0, act_bytes(Kmax)) : e;
   e = e == cudaSuccess ? cudaMemset(b.tickets, 0, (size_t)tick * 4) : e;
   e = e == cudaSuccess ? cudaMemset(b.argmax_tickets, 0, kMaxWidth * 4) : e;
+  e = e == cudaSuccess ? cudaMemset(b.attn_tickets, 0, (size_t)d.Hkv * 4) : e;
   e = e == cudaSuccess ? cudaMemset(b.ctl, 0, sizeof(SpecCtl)) : e;
   e = e == cudaSuccess ? cudaMemset(b.rec, 0, sizeof(AcceptRec)) : e;
   e = e == cudaSuccess ? cudaMemset(b.tree, 0, sizeof(TreeState)) : e;
