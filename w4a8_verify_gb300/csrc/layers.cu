@@ -62,7 +62,8 @@ __global__ void k_embed(SpecCtl* ctl, const TreeState* __restrict__ tree, int N,
 // Row statistics for RMSNorm, grid (token, slice of kQuantSlice inputs), 128 threads:
 // per slice the sum of squares (each thread its 4 inputs in order, a warp butterfly, the
 // 4 warps in order) and max |x|.
-__global__ void k_row_stats(const SpecCtl* ctl, float* __restrict__ x, int H, float2* __restrict__ part,
+__global__ void __launch_bounds__(kQuantSlice / 4)
+    k_row_stats(const SpecCtl* ctl, float* __restrict__ x, int H, float2* __restrict__ part,
                             const float* __restrict__ res, int res_S, const float* __restrict__ res_as) {
   griddep_enter();
   if (stopped(ctl)) return;
@@ -678,7 +679,8 @@ __global__ void k_attn_merge(const SpecCtl* ctl, const TreeState* __restrict__ t
 // grid (token, slice of kQuantSlice), 128 threads: h = silu(gate) * up written over the gate
 // half of the gate|up buffer, and the slice maximum of |h|.
 // gate and up rows come from the projection's EPI_PARTIAL slices (folded here).
-__global__ void k_swiglu(const SpecCtl* ctl, const float* __restrict__ gu_part, int gu_S, const float* __restrict__ a_s,
+__global__ void __launch_bounds__(kQuantSlice / 4)
+    k_swiglu(const SpecCtl* ctl, const float* __restrict__ gu_part, int gu_S, const float* __restrict__ a_s,
                          float* __restrict__ gu, int F, float2* __restrict__ part) {
   griddep_enter();
   if (stopped(ctl)) return;
@@ -711,21 +713,28 @@ constexpr int kArgmaxSlice = 8192;
 
 // grid (token, slice of kArgmaxSlice logits): slice maxima (ties -> lowest index), then the
 // last CTA of the token to finish (ticket) reduces the slice partials.
-__global__ void k_argmax(const SpecCtl* ctl, const float* __restrict__ logits, int V, float2* __restrict__ part,
-                         unsigned* __restrict__ tickets, int32_t* __restrict__ pred) {
+__global__ void __launch_bounds__(512)
+    k_argmax(const SpecCtl* ctl, const float* __restrict__ lpart, int lS, const float* __restrict__ a_s,
+                         float* __restrict__ logits, int V, float2* __restrict__ part, unsigned* __restrict__ tickets,
+                         int32_t* __restrict__ pred) {
   griddep_enter();
   if (stopped(ctl)) return;
   __shared__ float sv[32];
   __shared__ int si[32];
   __shared__ unsigned s_ticket;
   const int t = blockIdx.x, sl = blockIdx.y, ns = gridDim.y;
-  const float* lr = logits + (size_t)t * V;
+  float* lr = logits + (size_t)t * V;
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   const int k1 = min(V, (sl + 1) * kArgmaxSlice);
-  for (int k = sl * kArgmaxSlice + threadIdx.x; k < k1; k += blockDim.x) {
-    const float v = lr[k];
-    if (v > bv) { bv = v; bi = k; }
+  // the head projection's slices are folded here (V % 4 == 0); the logits are kept for readers
+  for (int k = sl * kArgmaxSlice + 4 * threadIdx.x; k < k1; k += 4 * blockDim.x) {
+    const float4 v = mm_fold4(lpart, lS, V, t, k, a_s);
+    *reinterpret_cast<float4*>(lr + k) = v;
+    if (v.x > bv) { bv = v.x; bi = k; }
+    if (v.y > bv) { bv = v.y; bi = k + 1; }
+    if (v.z > bv) { bv = v.z; bi = k + 2; }
+    if (v.w > bv) { bv = v.w; bi = k + 3; }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -879,9 +888,10 @@ cudaError_t launch_swiglu_quant(const DecoderBufs& b, const ModelDims& m, int N,
                     (const float*)b.gu, m.F, 2 * m.F, (const float2*)b.qpart, ns, 0.0f, b.act, N, b.a_s);
 }
 
-cudaError_t launch_argmax(const DecoderBufs& b, const ModelDims& m, int N, cudaStream_t st) {
+cudaError_t launch_argmax(const DecoderBufs& b, const ModelDims& m, int N, int lm_S, cudaStream_t st) {
   return launch_pdl(k_argmax, dim3(N, (m.V + kArgmaxSlice - 1) / kArgmaxSlice), dim3(512), 0, st,
-                    (const SpecCtl*)b.ctl, (const float*)b.logits, m.V, b.argmax_part, b.argmax_tickets, b.pred);
+                    (const SpecCtl*)b.ctl, (const float*)b.mm_part, lm_S, (const float*)b.a_s, b.logits, m.V,
+                    b.argmax_part, b.argmax_tickets, b.pred);
 }
 
 }  // namespace w4a8

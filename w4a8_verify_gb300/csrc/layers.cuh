@@ -18,7 +18,9 @@ cudaError_t launch_rope_kv(const DecoderBufs& b, const ModelDims& m, int N, int 
 cudaError_t launch_attention(const DecoderBufs& b, const ModelDims& m, int N, int layer, cudaStream_t st);
 // gate|up from the gu_S EPI_PARTIAL slices in b.mm_part
 cudaError_t launch_swiglu_quant(const DecoderBufs& b, const ModelDims& m, int N, int gu_S, cudaStream_t st);
-cudaError_t launch_argmax(const DecoderBufs& b, const ModelDims& m, int N, cudaStream_t st);
+// logits from the lm_S EPI_PARTIAL slices of the head projection in b.mm_part (folded here and
+// stored to b.logits)
+cudaError_t launch_argmax(const DecoderBufs& b, const ModelDims& m, int N, int lm_S, cudaStream_t st);
 
 // spec.cu
 cudaError_t launch_accept(const DecoderBufs& b, int N, int window_slot, cudaStream_t st);

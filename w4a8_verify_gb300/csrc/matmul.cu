@@ -25,7 +25,7 @@ namespace w4a8 {
 namespace {
 constexpr int kChunkBatch = 2;           // 64-input chunks per pipeline stage
 constexpr int kPersistentCtas = 304;     // fixed constant (2 x 152 SMs): part of the canonical schedule
-constexpr double kUnitFixedChunks = 6.0;  // modelled per-unit overhead, in chunk-streaming times
+constexpr double kUnitFixedChunks = 1.0;  // modelled per-unit overhead, in chunk-streaming times
 }  // namespace
 
 MatmulPlan mm_plan(int K, int N) {

@@ -51,16 +51,16 @@ cudaError_t mm_run(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, 
 // Four consecutive outputs (t, n .. n+3) (n % 4 == 0) of an EPI_PARTIAL matmul with S slices
 // and N rows: the slices folded left in ascending order and scaled, the same operations (and
 // bits) as the kernel's own fold and store.  Every slice's float4 is loaded before the sums
-// (up to 16 in flight).
+// (8 in flight).
 __device__ __forceinline__ float4 mm_fold4(const float* part, int S, int N, int t, int n, const float* a_s) {
   float4 f = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  for (int sb = 0; sb < S; sb += 16) {
-    float4 v[16];
+  for (int sb = 0; sb < S; sb += 8) {
+    float4 v[8];
 #pragma unroll
-    for (int q = 0; q < 16; ++q)
+    for (int q = 0; q < 8; ++q)
       if (sb + q < S) v[q] = *reinterpret_cast<const float4*>(part + ((size_t)(sb + q) * 16 + t) * N + n);
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
+    for (int q = 0; q < 8; ++q) {
       if (sb + q >= S) break;
       if (sb + q == 0) {
         f = v[q];

@@ -166,9 +166,9 @@ cudaError_t forward(w4a8_session* s, int N, bool head, float* logits_out, cudaSt
   }
   if (head) {
     TRYC(launch_rmsnorm_quant(b, d, N, res, res_S, st));
-    TRYC(mm_run(m->p_lm, m->lm_w, m->lm_s, b.act, b.a_s, N, b.logits, d.V, EPI_STORE, b.mm_part, b.tickets,
-                flags, flags, st));
-    TRYC(launch_argmax(b, d, N, st));
+    TRYC(mm_run(m->p_lm, m->lm_w, m->lm_s, b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets, flags,
+                flags, st));
+    TRYC(launch_argmax(b, d, N, m->p_lm.S, st));
     if (logits_out)
       TRYC(cudaMemcpyAsync(logits_out, b.logits, (size_t)N * d.V * sizeof(float), cudaMemcpyDeviceToDevice, st));
   }
@@ -299,9 +299,8 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
   b.max_window = desc->max_window;
   b.eos_id = desc->eos_id;
   const int Kmax = std::max(std::max(d.H, d.F), d.Hq * d.D);
-  // split-K scratch of the head projection (EPI_STORE) and the per-slice outputs of the layer
-  // projections (EPI_PARTIAL)
-  size_t part = std::max({m->p_lm.part_floats, mm_partial_floats(m->p_qkv), mm_partial_floats(m->p_o),
+  // per-slice outputs of the projections (EPI_PARTIAL)
+  size_t part = std::max({mm_partial_floats(m->p_lm), mm_partial_floats(m->p_qkv), mm_partial_floats(m->p_o),
                           mm_partial_floats(m->p_gu), mm_partial_floats(m->p_dn)});
   int tick = std::max({m->p_qkv.n_rg, m->p_o.n_rg, m->p_gu.n_rg, m->p_dn.n_rg, m->p_lm.n_rg});
   const size_t kv = (size_t)d.n_layers * d.Hkv * desc->kv_cap * d.D * sizeof(float);
@@ -716,8 +715,8 @@ W4A8_API w4a8_status w4a8_time_matmuls(w4a8_session* s, int N, int reps, double*
     launches += 4;
   }
   if (e3 == cudaSuccess)
-    e3 = mm_run(m->p_lm, m->lm_w, m->lm_s, b.act, b.a_s, N, b.logits, d.V, EPI_STORE, b.mm_part, b.tickets,
-                flags, flags, cs);
+    e3 = mm_run(m->p_lm, m->lm_w, m->lm_s, b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets, flags,
+                flags, cs);
   bytes += mbytes(m->p_lm);
   launches += 1;
   if (e == cudaSuccess) e = cudaStreamEndCapture(cs, &g);
