@@ -472,13 +472,45 @@ __global__ void __launch_bounds__(kAttnThreads)
             for (int d = 0; d < DL; ++d) Or[u][d] = Or[u][d] * cs;
             lmin = min(lmin, last[u]);
           }
+          // the row now holds the weights e (zero for a chunk beyond the node)
+          SP[(size_t)q * CH + lane] = e0[u];
+          SP[(size_t)q * CH + lane + 32] = e1[u];
         }
         lmax = max(lmax, last[u]);
       }
+      __syncwarp();
       // slots every active query sees, from the cache: no per-query tests (an inactive
       // query has e = 0 and its state is not stored); four slots per step
       const int jall = min(min(lmin + 1, jc), lmax + 1);
       int j = 0;
+      if (jall == CH) {
+        // whole cached chunk: constant trip count, weights read four at a time (broadcast)
+#pragma unroll
+        for (int jj = 0; jj < CH; jj += 4) {
+          float v[4][DL];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (DL == 4) {
+              const float4 t = *reinterpret_cast<const float4*>(Vs + (size_t)(jj + k) * D + d0);
+              v[k][0] = t.x; v[k][1 % DL] = t.y; v[k][2 % DL] = t.z; v[k][3 % DL] = t.w;
+            } else {
+              const float2 t = *reinterpret_cast<const float2*>(Vs + (size_t)(jj + k) * D + d0);
+              v[k][0] = t.x; v[k][1 % DL] = t.y;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < QT; ++u) {
+            const int q = min(warp + kAttnWarps * u, QN - 1);  // an inactive query's sums are discarded
+            const float4 e4 = *reinterpret_cast<const float4*>(SP + (size_t)q * CH + jj);
+            const float e[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+              for (int d = 0; d < DL; ++d) Or[u][d] = fmaf(e[k], v[k][d], Or[u][d]);
+          }
+        }
+        j = CH;
+      }
       auto vrow = [&](int jj, float (&v)[DL]) {
         if (DL == 4) {
           const float4 t = *reinterpret_cast<const float4*>(Vs + (size_t)jj * D + d0);
