@@ -429,7 +429,9 @@ def run_reference(args, rank, world):
         "vs_baseline": None,
         "dtype": "fp64 (oracle)",
         "data": "synthetic",
-        "config": {"workload": args.workload, "model": shape_name},
+        "config": {"workload": args.workload, "model": shape_name, "prompt_tokens": WORKLOADS[args.workload][1],
+                   "new_tokens_per_step": MAX_NEW, "widths": WIDTHS,
+                   "parallelism": "replicas" if world > 1 else "single"},
         "cpu_baseline": {"value": round(v, 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": "one plain greedy step of one decoder layer + 1/32 LM head per step, scaled"},
         "e2e": {"value": round(v, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
