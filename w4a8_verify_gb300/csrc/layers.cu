@@ -197,8 +197,8 @@ struct AttnLayout {
 __host__ __device__ inline AttnLayout attn_layout(int D, int QN) {
   AttnLayout a;
   a.stage = (size_t)2 * kAttnChunk * D * 4;         // ring entry 2s: K rows, 2s + 1: V rows
-  a.q = kAttnStages * a.stage;                       // queries [q][D]
-  a.kt = a.q + (size_t)QN * D * 4;                   // tree K rows [16][D]
+  a.q = kAttnStages * a.stage;                       // query A fragments [m-tile][k-step][lane] (hi, lo)
+  a.kt = a.q + (size_t)((QN + 15) / 16) * (D / 16) * 32 * 32;  // tree K rows [16][D]
   a.vt = a.kt + (size_t)kMaxWidth * D * 4;           // tree V rows
   a.sp = a.vt + (size_t)kMaxWidth * D * 4;           // scores [q][64]
   a.total = a.sp + (size_t)QN * kAttnChunk * 4;
@@ -219,14 +219,30 @@ __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(32 * kAttnWarps) : "memory");
 }
 
-// Quarter dot product of the score of (query row qr, key row kr) for quarter r of a key at
-// logical position p: dimensions r*DQ + ((t + rot) mod DQ), t ascending, with the rotation
-// rot = 4 * (((p & 1) << 2 | r)) mod DQ (a function of the position; it spreads the
-// shared-memory reads of a warp over the banks).
-template <int D>
-__device__ __forceinline__ int quarter_rot(int p, int r) {
-  return (4 * (((p & 1) << 2) | r)) % (D / 4);
+// f16 pair split of two floats: hi = rn(x), lo = rn(x - hi) (x - hi is exact in f32).
+__device__ __forceinline__ void split_h2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x, y);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(x - hf.x, y - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
+// d = A * B + d, m16n8k16, f16 inputs, f32 accumulation.
+__device__ __forceinline__ void mma_acc(float (&d)[4], uint4 a, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+// Score contribution of one 16-dimension step: three products of the f16 splits (hi*hi,
+// hi*lo, lo*hi, in this order) into the f32 accumulator.
+__device__ __forceinline__ void mma_split3(float (&d)[4], uint4 ahi, uint4 alo, uint32_t bh0, uint32_t bh1,
+                                           uint32_t bl0, uint32_t bl1) {
+  mma_acc(d, ahi, bh0, bh1);
+  mma_acc(d, ahi, bl0, bl1);
+  mma_acc(d, alo, bh0, bh1);
+}
+
 
 // Attention pass, grid (split sp, KV head kh).  Chunks of kAttnChunk logical positions are
 // dealt to the splits in contiguous ranges of R (R and the split count depend on the cache
@@ -234,8 +250,9 @@ __device__ __forceinline__ int quarter_rot(int p, int r) {
 // (contiguous) through a ring of 2 * kAttnStages cp.async.bulk entries and keeps, for every
 // query of the KV head (node i, head g; q = i*G + g), a running (M, L, O) over its chunks in
 // ascending order:
-//   scores: s = q . k as four quarter chains (quarter_rot order) added as (c0 + c1) + (c2 + c3);
-//           lane (slot j, quarter r) keeps its key quarter in registers and serves every query;
+//   scores: s = q . k on the tensor cores (mma m16n8k16, f32 accumulation) from the f16 splits
+//           q = qh + ql, k = kh + kl: per 16-dimension step qh.kh + qh.kl + ql.kh, steps in order
+//           (the row of a score depends on its own query and key only);
 //   per chunk: m = max(M, max over visible slots), c = exp(M - m), e_j = exp(s_j - m),
 //           L = L * c + (butterfly sum of e over the 64 slots), O[d] = O[d] * c, then
 //           O[d] = fmaf(e_j, v_j[d], O[d]) over the visible slots in ascending order; M = m.
@@ -252,8 +269,9 @@ __global__ void __launch_bounds__(kAttnThreads)
            float* __restrict__ o_part, float2* __restrict__ ml_part, unsigned* __restrict__ tickets,
            float* __restrict__ out, float2* __restrict__ mpart) {
   constexpr int CH = kAttnChunk;
-  constexpr int DQ = D / 4;          // quarter length
   constexpr int DL = D / 32;         // value dimensions per lane
+  constexpr int KS = D / 16;         // 16-dimension steps of a score
+  constexpr int MT = (kMaxWidth * G + 15) / 16 < (QT + 1) / 2 ? (kMaxWidth * G + 15) / 16 : (QT + 1) / 2;
   constexpr int NE = 2 * kAttnStages;  // ring entries (K or V rows of one chunk)
   static_assert(D == 64 || D == 128, "head size");
   // The committed length, the tree shape and the cached rows below it were written by
@@ -275,7 +293,7 @@ __global__ void __launch_bounds__(kAttnThreads)
   const int nsa = (nch + R - 1) / R;  // CTAs of this head that hold chunks
   const int QN = N * G;
   const AttnLayout lay = attn_layout(D, QN);
-  float* Qs = reinterpret_cast<float*>(smem + lay.q);
+  uint8_t* Qf = smem + lay.q;
   float* Kt = reinterpret_cast<float*>(smem + lay.kt);
   float* Vt = reinterpret_cast<float*>(smem + lay.vt);
   float* SP = reinterpret_cast<float*>(smem + lay.sp);
@@ -350,11 +368,35 @@ __global__ void __launch_bounds__(kAttnThreads)
   }
   // queries of the KV head (the G heads of kh are consecutive in qrot) and the tree rows
   // (slots L .. L+N-1, read by the chunks that reach past L)
-  for (int idx = threadIdx.x; idx < QN * D / 4; idx += 32 * kAttnWarps) {
-    const int q = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
-    const int i = q / G, g = q % G;
-    *reinterpret_cast<float4*>(Qs + (size_t)q * D + d4) =
-        *reinterpret_cast<const float4*>(qrot + ((size_t)i * Hq + kh * G + g) * D + d4);
+  // A fragments of m16n8k16 (rows = queries, columns = dimensions), split into f16 hi and lo:
+  // lane (g, t) of m-tile mt, step s holds rows g, g+8 and columns 2t, 2t+1, 2t+8, 2t+9
+  {
+    const int nmt = (QN + 15) / 16;
+    for (int idx = threadIdx.x; idx < nmt * KS * 32; idx += 32 * kAttnWarps) {
+      const int ln = idx & 31, st = (idx >> 5) % KS, mt = (idx >> 5) / KS;
+      const int g = ln >> 2, t = ln & 3;
+      float v[8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int q = mt * 16 + g + 8 * h;
+        if (q < QN) {
+          const float* qr = qrot + ((size_t)(q / G) * Hq + kh * G + q % G) * D + st * 16 + 2 * t;
+          const float2 lo2 = *reinterpret_cast<const float2*>(qr);
+          const float2 hi2 = *reinterpret_cast<const float2*>(qr + 8);
+          v[2 * h] = lo2.x; v[2 * h + 1] = lo2.y; v[4 + 2 * h] = hi2.x; v[5 + 2 * h] = hi2.y;
+        } else {
+          v[2 * h] = v[2 * h + 1] = v[4 + 2 * h] = v[5 + 2 * h] = 0.0f;
+        }
+      }
+      uint4 ah, al;  // registers a0 (row g), a1 (row g+8), a2 (row g, +8 columns), a3 (row g+8, +8)
+      split_h2(v[0], v[1], ah.x, al.x);
+      split_h2(v[2], v[3], ah.y, al.y);
+      split_h2(v[4], v[5], ah.z, al.z);
+      split_h2(v[6], v[7], ah.w, al.w);
+      uint4* dst = reinterpret_cast<uint4*>(Qf + ((size_t)(mt * KS + st) * 32 + ln) * 32);
+      dst[0] = ah;
+      dst[1] = al;
+    }
   }
   for (int idx = threadIdx.x; idx < N * D / 4; idx += 32 * kAttnWarps) {
     reinterpret_cast<float4*>(Kt)[idx] = reinterpret_cast<const float4*>(kb + (size_t)L * D)[idx];
@@ -386,53 +428,74 @@ __global__ void __launch_bounds__(kAttnThreads)
     const int P0 = c * CH;
     const int jc = min(CH, L - P0);  // slots below jc come from the cache
 
-    // ---- scores: lane (slot j, quarter r) over all queries, four at a time
+    // ---- scores on the tensor cores: warp w takes keys 8w..8w+7 (one n-tile) for every m-tile
+    // of queries; a score is the sum over 16-dimension steps of hi*hi + hi*lo + lo*hi of the
+    // f16 splits of the query and the key, accumulated in f32 in that fixed order.
     {
-      const int j = 8 * warp + (lane >> 2), r = lane & 3;
-      const int p = P0 + j;
-      const int rot = quarter_rot<D>(p, r);
-      float kq[DQ];  // kq[t] = K[j][r*DQ + (t + rot) % DQ]
-      if (j < jc) {
+      const int g = lane >> 2, t = lane & 3;
+      const int nmt = (QN + 15) / 16;
+      const int j = 8 * warp + g;  // key of this lane's B fragment
+      auto store = [&](const float (&acc)[4], int mt, int node) {
+        // node < 0: every row; else only the rows of that node
 #pragma unroll
-        for (int t = 0; t < DQ; t += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(Ks + (size_t)j * D + r * DQ + ((t + rot) % DQ));
-          kq[t] = v.x; kq[t + 1] = v.y; kq[t + 2] = v.z; kq[t + 3] = v.w;
+        for (int e = 0; e < 4; ++e) {
+          const int q = mt * 16 + g + ((e & 2) ? 8 : 0);
+          const int key = 8 * warp + 2 * t + (e & 1);
+          if (q >= QN || (node >= 0 && q / G != node)) continue;
+          const int p = P0 + key;
+          SP[(size_t)q * CH + key] = (p <= L + s_dep[q / G]) ? acc[e] : -INFINITY;
         }
-      }
-      for (int q0 = 0; q0 < QN; q0 += 4) {
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (j < jc) {
+      };
+      if (8 * warp + 7 < jc) {  // every key of the n-tile is cached: one B for all queries
+        float acc[MT][4];
 #pragma unroll
-          for (int t = 0; t < DQ; t += 4) {
-            const int dd = r * DQ + ((t + rot) % DQ);
+        for (int m = 0; m < MT; ++m)
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float4 qv = *reinterpret_cast<const float4*>(Qs + (size_t)min(q0 + u, QN - 1) * D + dd);
-              acc[u] = fmaf(qv.x, kq[t], acc[u]);
-              acc[u] = fmaf(qv.y, kq[t + 1], acc[u]);
-              acc[u] = fmaf(qv.z, kq[t + 2], acc[u]);
-              acc[u] = fmaf(qv.w, kq[t + 3], acc[u]);
+          for (int e = 0; e < 4; ++e) acc[m][e] = 0.0f;
+#pragma unroll
+        for (int st = 0; st < KS; ++st) {
+          const float* kr = Ks + (size_t)j * D + st * 16 + 2 * t;
+          const float2 k0 = *reinterpret_cast<const float2*>(kr);
+          const float2 k1 = *reinterpret_cast<const float2*>(kr + 8);
+          uint32_t bh0, bl0, bh1, bl1;
+          split_h2(k0.x, k0.y, bh0, bl0);
+          split_h2(k1.x, k1.y, bh1, bl1);
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            if (m >= nmt) break;
+            const uint4* af = reinterpret_cast<const uint4*>(Qf + ((size_t)(m * KS + st) * 32 + lane) * 32);
+            mma_split3(acc[m], af[0], af[1], bh0, bh1, bl0, bl1);
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+          if (m < nmt) store(acc[m], m, -1);
+      } else {
+        // n-tile reaching past the cache: keys at L + e are each node's ancestors, so every
+        // node takes its own B (cached keys are the same rows for all nodes)
+        const int p = P0 + j;
+        for (int node = 0; node < N; ++node) {
+          const float* kr = nullptr;
+          if (j < jc) kr = Ks + (size_t)j * D;
+          else if (p - L <= s_dep[node]) kr = Kt + (size_t)s_path[node][p - L] * D;
+          const int m_lo = (node * G) / 16, m_hi = (node * G + G - 1) / 16;
+          for (int m = m_lo; m <= m_hi; ++m) {
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int st = 0; st < KS; ++st) {
+              float2 k0 = make_float2(0.0f, 0.0f), k1 = make_float2(0.0f, 0.0f);
+              if (kr != nullptr) {
+                k0 = *reinterpret_cast<const float2*>(kr + st * 16 + 2 * t);
+                k1 = *reinterpret_cast<const float2*>(kr + st * 16 + 2 * t + 8);
+              }
+              uint32_t bh0, bl0, bh1, bl1;
+              split_h2(k0.x, k0.y, bh0, bl0);
+              split_h2(k1.x, k1.y, bh1, bl1);
+              const uint4* af = reinterpret_cast<const uint4*>(Qf + ((size_t)(m * KS + st) * 32 + lane) * 32);
+              mma_split3(acc, af[0], af[1], bh0, bh1, bl0, bl1);
             }
+            store(acc, m, node);
           }
-        } else {
-          // tree slot: the key row is the ancestor of each query's node at depth p - L
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int q = min(q0 + u, QN - 1), i = q / G;
-            if (p - L > s_dep[i]) continue;
-            const float* kr = Kt + (size_t)s_path[i][p - L] * D + r * DQ;
-            const float* qr = Qs + (size_t)q * D + r * DQ;
-            float a = 0.0f;
-            for (int t = 0; t < DQ; ++t) a = fmaf(qr[(t + rot) % DQ], kr[(t + rot) % DQ], a);
-            acc[u] = a;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float sc = acc[u] + __shfl_xor_sync(0xffffffffu, acc[u], 1);
-          sc = sc + __shfl_xor_sync(0xffffffffu, sc, 2);
-          const int q = q0 + u;
-          if (r == 0 && q < QN) SP[(size_t)q * CH + j] = (p <= L + s_dep[q / G]) ? sc : -INFINITY;
         }
       }
     }
