@@ -96,40 +96,20 @@ __global__ void __launch_bounds__(kQuantSlice / 4)
                                                    fmaxf(fmaxf(s_mx[0], s_mx[1]), fmaxf(s_mx[2], s_mx[3])));
 }
 
-// Quantisation pass, grid (token, slice), 128 threads, one 4-input quad per thread.  The
-// per-token scale comes from the slice partials (fixed order): mode 0 plain (amax = max of
-// the partial maxima), mode 1 RMSNorm (x scaled by r = 1/sqrt(sum of squares / K + eps), and
-// amax = max |x| * r, equal to the maximum of the rounded products since rounding is monotone).
-template <int MODE>
-__global__ void k_quant_slices(const SpecCtl* ctl, const float* __restrict__ x, int K, int ldx,
-                               const float2* __restrict__ part, int nparts, float eps, uint8_t* act, int M,
-                               float* a_s) {
-  griddep_enter();
-  if (stopped(ctl)) return;
-  const int t = blockIdx.x, sl = blockIdx.y;
-  float mx = 0.0f, r = 1.0f;
-  if (MODE == 1) {
-    float ss = 0.0f;
-    for (int p = 0; p < nparts; ++p) {
-      const float2 v = part[(size_t)t * nparts + p];
-      ss = ss + v.x;
-      mx = fmaxf(mx, v.y);
-    }
-    r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
-    mx = mx * r;
-  } else {
-    for (int p = 0; p < nparts; ++p) mx = fmaxf(mx, part[(size_t)t * nparts + p].y);
-  }
-  const float s = __fdiv_rn(mx, 127.0f);
-  const int NT = act_tiles(M);
-  const int k = sl * kQuantSlice + 4 * threadIdx.x;
-  const bool active = k < K;  // K % 32 == 0: groups of 8 lanes are all active or all idle
-  const bool pad = !active && k < chunks_of(K) * 64;  // the zero group that completes the last chunk
+// Quantiser scale of token t from slice maxima (the exact maximum of the partial maxima).
+__device__ __forceinline__ float quant_scale_max(const float2* part, int t, int nparts) {
+  float mx = 0.0f;
+  for (int p = 0; p < nparts; ++p) mx = fmaxf(mx, __ldcg(part + (size_t)t * nparts + p).y);
+  return __fdiv_rn(mx, 127.0f);
+}
+
+// int8 codes of the quad (inputs k..k+3 of token t) into the activation records.  Called by a
+// whole warp: lanes 8m..8m+7 hold the 32 inputs of one group (their sum seeds the group).
+__device__ __forceinline__ void quant_quad(float4 v, float s, bool active, bool pad, int t, int k, uint8_t* act,
+                                           int NT) {
   uint32_t codes = 0;
   int sum = 0;
   if (active) {
-    float4 v = *reinterpret_cast<const float4*>(x + (size_t)t * ldx + k);
-    if (MODE == 1) { v.x = v.x * r; v.y = v.y * r; v.z = v.z * r; v.w = v.w * r; }
     const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
@@ -144,6 +124,41 @@ __global__ void k_quant_slices(const SpecCtl* ctl, const float* __restrict__ x, 
   sum += __shfl_xor_sync(0xffffffffu, sum, 2);
   sum += __shfl_xor_sync(0xffffffffu, sum, 4);
   if ((active || pad) && (threadIdx.x & 7) == 0) act_store_corr(act, NT, t, k >> 5, sum);
+}
+
+// Quantisation pass, grid (token, slice), 128 threads, one 4-input quad per thread.  The
+// per-token scale comes from the slice partials (fixed order): mode 0 plain (amax = max of
+// the partial maxima), mode 1 RMSNorm (x scaled by r = 1/sqrt(sum of squares / K + eps), and
+// amax = max |x| * r, equal to the maximum of the rounded products since rounding is monotone).
+template <int MODE>
+__global__ void k_quant_slices(const SpecCtl* ctl, const float* __restrict__ x, int K, int ldx,
+                               const float2* __restrict__ part, int nparts, float eps, uint8_t* act, int M,
+                               float* a_s) {
+  griddep_enter();
+  if (stopped(ctl)) return;
+  const int t = blockIdx.x, sl = blockIdx.y;
+  float s, r = 1.0f;
+  if (MODE == 1) {
+    float mx = 0.0f, ss = 0.0f;
+    for (int p = 0; p < nparts; ++p) {
+      const float2 v = part[(size_t)t * nparts + p];
+      ss = ss + v.x;
+      mx = fmaxf(mx, v.y);
+    }
+    r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
+    s = __fdiv_rn(mx * r, 127.0f);
+  } else {
+    s = quant_scale_max(part, t, nparts);
+  }
+  const int k = sl * kQuantSlice + 4 * threadIdx.x;
+  const bool active = k < K;  // K % 32 == 0: groups of 8 lanes are all active or all idle
+  const bool pad = !active && k < chunks_of(K) * 64;  // the zero group that completes the last chunk
+  float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (active) {
+    v = *reinterpret_cast<const float4*>(x + (size_t)t * ldx + k);
+    if (MODE == 1) { v.x = v.x * r; v.y = v.y * r; v.z = v.z * r; v.w = v.w * r; }
+  }
+  quant_quad(v, s, active, pad, t, k, act, act_tiles(M));
   if (sl == 0 && threadIdx.x == 0) a_s[t] = s;
 }
 
