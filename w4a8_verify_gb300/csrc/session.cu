@@ -96,10 +96,12 @@ struct w4a8_session {
   int next_slot = 0;
   std::map<long long, cudaGraphExec_t> graphs;
   std::map<long long, int> graph_kernels;  // kernel nodes of each window graph
+  cudaGraphExec_t chain_graph = nullptr;   // one prefill chain of kMaxWidth prompt tokens
   long long host_syncs = 0;
   long long kernels = 0;                   // kernels launched by window graphs
   ~w4a8_session() {
     for (auto& kv : graphs) cudaGraphExecDestroy(kv.second);
+    if (chain_graph) cudaGraphExecDestroy(chain_graph);
     for (int i = 0; i < 2; ++i)
       if (ev[i]) cudaEventDestroy(ev[i]);
     if (cap) cudaStreamDestroy(cap);
@@ -379,11 +381,31 @@ W4A8_API w4a8_status w4a8_prefill(w4a8_session* s, const int32_t* prompt, int n,
   cudaStream_t st = as_stream(stream);
   W4A8_CUDA_TRY(cudaMemcpyAsync(b.ctx, prompt, (size_t)n * 4, cudaMemcpyDeviceToDevice, st));
   W4A8_CUDA_TRY(launch_pdl(k_init_ctl, dim3(1), dim3(32), 0, st, b.ctl, b.rec, (const int32_t*)b.ctx, n, max_new));
-  for (int start = 0; start < n - 1; start += kMaxWidth) {
-    const int len = std::min(kMaxWidth, n - 1 - start);
-    W4A8_CUDA_TRY(launch_chain_tree(b, start, len, st));
-    W4A8_CUDA_TRY(forward(s, len, false, nullptr, st));
-    W4A8_CUDA_TRY(launch_commit_chain(b, len, st));
+  // Full chains replay one captured graph (the chain kernels read their position from the
+  // control word); the last, shorter chain is launched directly.
+  const int full = (n - 1) / kMaxWidth;
+  if (full > 0 && !s->chain_graph) {
+    cudaGraph_t g = nullptr;
+    W4A8_CUDA_TRY(cudaStreamBeginCapture(s->cap, cudaStreamCaptureModeThreadLocal));
+    cudaError_t e = launch_chain_tree(b, 0, kMaxWidth, s->cap);
+    if (e == cudaSuccess) e = forward(s, kMaxWidth, false, nullptr, s->cap);
+    if (e == cudaSuccess) e = launch_commit_chain(b, kMaxWidth, s->cap);
+    const cudaError_t e2 = cudaStreamEndCapture(s->cap, &g);
+    if (e == cudaSuccess) e = e2;
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&s->chain_graph, g, 0);
+    if (g) cudaGraphDestroy(g);
+    if (e != cudaSuccess) {
+      s->chain_graph = nullptr;
+      (void)cudaGetLastError();
+      return W4A8_ERR_CUDA;
+    }
+  }
+  for (int c = 0; c < full; ++c) W4A8_CUDA_TRY(cudaGraphLaunch(s->chain_graph, st));
+  const int rest = n - 1 - full * kMaxWidth;
+  if (rest > 0) {
+    W4A8_CUDA_TRY(launch_chain_tree(b, full * kMaxWidth, rest, st));
+    W4A8_CUDA_TRY(forward(s, rest, false, nullptr, st));
+    W4A8_CUDA_TRY(launch_commit_chain(b, rest, st));
   }
   W4A8_CUDA_TRY(launch_draft(b, 1, st));
   return W4A8_OK;
