@@ -66,6 +66,17 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
 }
 
+// (c0, c1) = (a * b0 + c0, a * b1 + c1): two fmaf (single rounding each) in one packed f32x2
+// instruction.
+__device__ __forceinline__ void fma2(float& c0, float& c1, float a, float b0, float b1) {
+  uint64_t c = ((uint64_t)__float_as_uint(c1) << 32) | __float_as_uint(c0);
+  const uint64_t aa = ((uint64_t)__float_as_uint(a) << 32) | __float_as_uint(a);
+  const uint64_t bb = ((uint64_t)__float_as_uint(b1) << 32) | __float_as_uint(b0);
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(c) : "l"(aa), "l"(bb));
+  c0 = __uint_as_float((uint32_t)c);
+  c1 = __uint_as_float((uint32_t)(c >> 32));
+}
+
 // The four A-fragment registers of one weight word (see layout.cuh).
 __device__ __forceinline__ void unpack_codes(uint32_t x, uint32_t (&r)[4]) {
   r[0] = x & 0x000F000Fu;
@@ -138,10 +149,8 @@ __device__ __forceinline__ void mm_chunks(const uint8_t* stage, int u0, int rl0,
       for (int gg = 0; gg < 2; ++gg)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          acc[r][nt][0] = fmaf(sg[gg].x, d[gg][nt][0], acc[r][nt][0]);
-          acc[r][nt][1] = fmaf(sg[gg].x, d[gg][nt][1], acc[r][nt][1]);
-          acc[r][nt][2] = fmaf(sg[gg].y, d[gg][nt][2], acc[r][nt][2]);
-          acc[r][nt][3] = fmaf(sg[gg].y, d[gg][nt][3], acc[r][nt][3]);
+          fma2(acc[r][nt][0], acc[r][nt][1], sg[gg].x, d[gg][nt][0], d[gg][nt][1]);
+          fma2(acc[r][nt][2], acc[r][nt][3], sg[gg].y, d[gg][nt][2], d[gg][nt][3]);
         }
     }
   }
