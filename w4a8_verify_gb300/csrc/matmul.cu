@@ -110,48 +110,39 @@ __device__ __forceinline__ void mm_chunks(const uint8_t* stage, int u0, int rl0,
 #pragma unroll
   for (int u = u0; u < u0 + NCH; ++u) {
     const uint8_t* sa = stage + kStageA0 + u * rec;
-    uint4 bf[2][NT];
-    float4 cq[2][NT];
+    // group gg of the chunk: every row block's accumulators take group 0 before group 1
 #pragma unroll
-    for (int gg = 0; gg < 2; ++gg)
+    for (int gg = 0; gg < 2; ++gg) {
+      uint4 bf[NT];
+      float4 cq[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        bf[gg][nt] = reinterpret_cast<const uint4*>(sa + (nt * 2 + gg) * 512)[lane];
-        cq[gg][nt] = reinterpret_cast<const float4*>(sa + NT * 1024 + (gg * NT + nt) * 64)[tig];
+        bf[nt] = reinterpret_cast<const uint4*>(sa + (nt * 2 + gg) * 512)[lane];
+        cq[nt] = reinterpret_cast<const float4*>(sa + NT * 1024 + (gg * NT + nt) * 64)[tig];
       }
 #pragma unroll
-    for (int r = 0; r < kRowBlocksPerWarp; ++r) {
-      const int rl = rl0 + r;
-      const uint4 wv = reinterpret_cast<const uint4*>(stage + u * kChunkW + rl * 512)[lane];
-      const uint2 sv = reinterpret_cast<const uint2*>(stage + kStageS0 + u * kChunkS + rl * 64)[gid];
-      float2 sg[2];
-      sg[0] = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));  // (row gid, row gid+8), group 0
-      sg[1] = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));
-      uint32_t wa[2][4], wb[2][4];  // [group][register] of rows gid and gid+8
-      unpack_codes(wv.x, wa[0]);
-      unpack_codes(wv.y, wb[0]);
-      unpack_codes(wv.z, wa[1]);
-      unpack_codes(wv.w, wb[1]);
-      float d[2][NT][4];
-#pragma unroll
-      for (int gg = 0; gg < 2; ++gg)
+      for (int r = 0; r < kRowBlocksPerWarp; ++r) {
+        const int rl = rl0 + r;
+        // words (rows gid, gid+8) of group gg, and the group's scales of those rows
+        const uint2 wv = reinterpret_cast<const uint2*>(stage + u * kChunkW + rl * 512)[2 * lane + gg];
+        const uint32_t sv = reinterpret_cast<const uint32_t*>(stage + kStageS0 + u * kChunkS + rl * 64)[2 * gid + gg];
+        const float2 sg = __half22float2(*reinterpret_cast<const __half2*>(&sv));
+        uint32_t wa[4], wb[4];
+        unpack_codes(wv.x, wa);
+        unpack_codes(wv.y, wb);
+        float d[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
-          mma_f16(d[gg][nt], wa[gg][0], wb[gg][0], wa[gg][1], wb[gg][1], bf[gg][nt].x, bf[gg][nt].y,
-                  cq[gg][nt].x, cq[gg][nt].y, cq[gg][nt].z, cq[gg][nt].w);
-#pragma unroll
-      for (int gg = 0; gg < 2; ++gg)
+          mma_f16(d[nt], wa[0], wb[0], wa[1], wb[1], bf[nt].x, bf[nt].y, cq[nt].x, cq[nt].y, cq[nt].z, cq[nt].w);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
-          mma_f16(d[gg][nt], wa[gg][2], wb[gg][2], wa[gg][3], wb[gg][3], bf[gg][nt].z, bf[gg][nt].w,
-                  d[gg][nt][0], d[gg][nt][1], d[gg][nt][2], d[gg][nt][3]);
-#pragma unroll
-      for (int gg = 0; gg < 2; ++gg)
+          mma_f16(d[nt], wa[2], wb[2], wa[3], wb[3], bf[nt].z, bf[nt].w, d[nt][0], d[nt][1], d[nt][2], d[nt][3]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          fma2(acc[r][nt][0], acc[r][nt][1], sg[gg].x, d[gg][nt][0], d[gg][nt][1]);
-          fma2(acc[r][nt][2], acc[r][nt][3], sg[gg].y, d[gg][nt][2], d[gg][nt][3]);
+          fma2(acc[r][nt][0], acc[r][nt][1], sg.x, d[nt][0], d[nt][1]);
+          fma2(acc[r][nt][2], acc[r][nt][3], sg.y, d[nt][2], d[nt][3]);
         }
+      }
     }
   }
 }
