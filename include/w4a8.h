@@ -326,6 +326,18 @@ w4a8_status w4a8_session_get_tree(w4a8_session* s, int32_t* tok, int32_t* parent
 w4a8_status w4a8_session_get_pred(w4a8_session* s, int32_t* pred, int n);
 /* Copies the context tokens (host int32[cap]); *n = context length. */
 w4a8_status w4a8_session_get_context(w4a8_session* s, int32_t* out, int cap, int* n);
+/* Tree attention of one layer alone [P1 GPU-Resident Speculation Loop: each node attends to
+ * the committed cache and to its ancestors], on the session's cache, committed length L and tree,
+ * for caller-supplied queries: node i (0 <= i < n) attends to cache slots [0, L) and to the
+ * slots L + a of its ancestors-or-self a, with softmax weights over q . k.
+ * q: device fp32 [n][n_heads][head_dim], queries after RoPE and the 1/sqrt(head_dim) scale
+ * (query head h uses KV head h / (n_heads / n_kv_heads)); out: device fp32
+ * [n][n_heads * head_dim].  Slots L .. L+n-1 must hold the nodes' K/V (tree_verify_step
+ * writes them).  Synchronises the stream to read the control state: W4A8_ERR_DEVICE_FLAG
+ * if a stop or error flag is set, W4A8_ERR_CAPACITY if L + n > kv_cap, W4A8_ERR_ARG if
+ * n exceeds the tree's valid nodes.  Overwrites the session's query and attention
+ * scratch buffers (tests and tools). */
+w4a8_status w4a8_session_attention(w4a8_session* s, int layer, int n, const float* q, float* out, void* stream);
 /* Device.  Copies K and V of one layer, slots [slot0, slot0+n), into k_out/v_out (device
  * fp32 [n_kv_heads][n][head_dim]). */
 w4a8_status w4a8_session_copy_kv(w4a8_session* s, int layer, int slot0, int n, float* k_out, float* v_out,

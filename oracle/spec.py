@@ -34,7 +34,7 @@ import heapq
 
 import numpy as np
 
-from .model import Model, argmax_lowest
+from .model import Model, argmax_lowest, attend, kv_head_of
 
 MAX_ORDER = 8
 N_CAND = 16
@@ -59,12 +59,36 @@ def ancestors_or_self(parent, i) -> list:
     return path[::-1]
 
 
+def tree_visible(L_c: int, parent, i: int) -> list:
+    """Cache slots node i sees in a verification step: [0, L_c), then the slots L_c + a of
+    its root path (a node's K/V sits at slot L_c + its index)."""
+    return list(range(L_c)) + [L_c + a for a in ancestors_or_self(parent, i)]
+
+
+def tree_attention(qs: np.ndarray, K: np.ndarray, V: np.ndarray, L_c: int, parent) -> np.ndarray:
+    """Attention of every tree node over the slots it sees (Design > GPU-Resident
+    Speculation Loop: each node attends to the committed cache and to its ancestors).
+    qs: [n][Hq][d] queries already multiplied by 1/sqrt(d); K, V: [Hkv][slots][d].
+    Returns fp64 [n][Hq][d]: softmax(qs . k) v over the visible slots, query head h
+    reading KV head h // (Hq / Hkv)."""
+    n, Hq, d = qs.shape
+    Hkv = K.shape[0]
+    out = np.zeros((n, Hq, d))
+    for i in range(n):
+        vis = np.asarray(tree_visible(L_c, parent, i), dtype=np.int64)
+        for h in range(Hq):
+            kh = kv_head_of(h, Hq, Hkv)
+            # attend divides the scores by sqrt(d): undo the factor the queries carry
+            out[i, h] = attend(np.asarray(qs[i, h], dtype=np.float64) * np.sqrt(d), K[kh, vis], V[kh, vis])
+    return out
+
+
 def tree_verify(model: Model, L_c: int, tok, parent) -> np.ndarray:
     """Logits of every tree node; node i sits at logical position L_c + depth(i), writes
     its K/V to slot L_c + i and sees cache slots [0, L_c) then its root path."""
     depth = tree_depths(parent)
     n = len(tok)
-    vis = [list(range(L_c)) + [L_c + a for a in ancestors_or_self(parent, i)] for i in range(n)]
+    vis = [tree_visible(L_c, parent, i) for i in range(n)]
     return model.forward(list(tok), [L_c + int(depth[i]) for i in range(n)],
                          [L_c + i for i in range(n)], vis)
 

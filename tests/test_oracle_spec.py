@@ -204,3 +204,66 @@ def test_max_new_truncates_and_eos_stops(tiny):
     eos = greedy[3]
     out, _ = OS.spec_decode(w, prompt, 32, 8, eos=eos)
     assert out == greedy[:greedy.index(eos) + 1]
+
+
+# ------------------------------------------------------------------ tree attention pins
+
+def _attn_case(seed, n_heads=4, n_kv=2, d=8, L=5, n=6):
+    rng = np.random.default_rng(seed)
+    K = rng.standard_normal((n_kv, L + n, d))
+    V = rng.standard_normal((n_kv, L + n, d))
+    qs = rng.standard_normal((n, n_heads, d)) / np.sqrt(d)
+    return qs, K, V
+
+
+def test_tree_attention_chain_is_causal_attention():
+    # a chain's node i sees every slot up to L + i: plain causal softmax attention, written out
+    qs, K, V = _attn_case(1)
+    L, n = 5, 6
+    out = OS.tree_attention(qs, K, V, L, [-1] + list(range(n - 1)))
+    for i in range(n):
+        for h in range(4):
+            kh = h // 2
+            sc = K[kh, :L + i + 1] @ qs[i, h]
+            w = np.exp(sc - sc.max())
+            assert np.allclose(out[i, h], (w / w.sum()) @ V[kh, :L + i + 1], rtol=1e-12, atol=1e-12)
+
+
+def test_tree_attention_star_sees_root_and_itself():
+    # every node a child of the root: node i sees [0, L), slot L (root) and slot L + i
+    qs, K, V = _attn_case(2)
+    L, n = 5, 6
+    out = OS.tree_attention(qs, K, V, L, [-1] + [0] * (n - 1))
+    for i in range(1, n):
+        vis = [0, 1, 2, 3, 4, L, L + i]
+        for h in range(4):
+            kh = h // 2
+            sc = K[kh, vis] @ qs[i, h]
+            w = np.exp(sc - sc.max())
+            assert np.allclose(out[i, h], (w / w.sum()) @ V[kh, vis], rtol=1e-12, atol=1e-12)
+
+
+def test_tree_attention_ignores_slots_off_the_path():
+    # tree 0 -> 1 -> 3, 0 -> 2: node 3 must not see node 2's slot; node 2 must not see 1 or 3
+    qs, K, V = _attn_case(3, n=4)
+    L = 5
+    parent = [-1, 0, 0, 1]
+    base = OS.tree_attention(qs, K, V, L, parent)
+    K2, V2 = K.copy(), V.copy()
+    K2[:, L + 2] += 5.0
+    V2[:, L + 2] -= 3.0
+    moved = OS.tree_attention(qs, K2, V2, L, parent)
+    assert np.array_equal(base[3], moved[3]) and np.array_equal(base[1], moved[1])
+    assert not np.allclose(base[2], moved[2])
+    K3 = K.copy()
+    K3[:, L + 1] += 5.0  # an ancestor of node 3: its output changes
+    assert not np.allclose(OS.tree_attention(qs, K3, V, L, parent)[3], base[3])
+
+
+def test_tree_attention_uses_the_grouped_kv_head():
+    # V of KV head 1 zeroed: query heads 2, 3 (group of KV head 1) give zero, heads 0, 1 do not
+    qs, K, V = _attn_case(4)
+    V[1] = 0.0
+    out = OS.tree_attention(qs, K, V, 5, [-1, 0, 1, 1, 0, 4])
+    assert np.all(out[:, 2:] == 0.0)
+    assert np.all(np.abs(out[:, :2]).sum(axis=-1) > 0)

@@ -100,6 +100,7 @@ _SIGNATURES = {
     "w4a8_session_get_pred": [_vp, _c.POINTER(_i32), _i32],
     "w4a8_session_get_context": [_vp, _c.POINTER(_i32), _i32, _c.POINTER(_i32)],
     "w4a8_session_copy_kv": [_vp, _i32, _i32, _i32, _vp, _vp, _vp],
+    "w4a8_session_attention": [_vp, _i32, _i32, _vp, _vp, _vp],
     "w4a8_controller_create": [_c.POINTER(_i32), _c.POINTER(_f32), _i32, _c.POINTER(_vp)],
     "w4a8_controller_destroy": [_vp],
     "w4a8_controller_choose": [_vp],
@@ -416,6 +417,11 @@ class Session:
     def copy_kv(self, layer, slot0, n, k_out, v_out, stream=None):
         _call("w4a8_session_copy_kv", self.h, int(layer), int(slot0), int(n), _ptr(k_out), _ptr(v_out),
               _stream(stream))
+
+    def attention(self, layer, n, q, out, stream=None):
+        """Tree attention of one layer for device queries q [n][n_heads][head_dim] (after RoPE
+        and the 1/sqrt(head_dim) scale) into out [n][n_heads * head_dim] (w4a8_session_attention)."""
+        _call("w4a8_session_attention", self.h, int(layer), int(n), _ptr(q), _ptr(out), _stream(stream))
 
 
 class Controller:

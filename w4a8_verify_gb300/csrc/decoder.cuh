@@ -90,6 +90,9 @@ struct DecoderBufs {
   int32_t* wtok;          // [max_window][16] emitted tokens per step of the window
   int kv_cap, ctx_cap, n_chunks, max_window;
   int eos_id;
+  // TMA maps of the K and V caches, dims {D, kv_cap, Hkv, layers}; a box is one attention
+  // chunk of 64 rows landing at the padded shared-memory row strides
+  CUtensorMap tm_k, tm_v;
 };
 
 }  // namespace w4a8

@@ -204,19 +204,28 @@ __global__ void k_rope_kv(const SpecCtl* ctl, const TreeState* __restrict__ tree
 constexpr int kAttnStages = 2;                      // chunks in flight (K and V entries of 64 rows each)
 constexpr int kAttnWarps = 8;                       // compute warps; one more warp issues the copies
 constexpr int kAttnThreads = 32 * (kAttnWarps + 1);
+constexpr float kAttnEScale = 32768.0f;             // 2^15: weights e in [0, 1] enter the value product scaled
+// Shared-memory row strides (floats) of a ring entry: key rows D + 8 and value rows D + 4, so
+// that the B fragments (rows 2t.., columns g) of the tensor-core steps fall on distinct banks;
+// score rows kAttnChunk + 8, so that the float2 score stores of a fragment do as well.
+__host__ __device__ constexpr int attn_kstr(int D) { return D + 8; }
+__host__ __device__ constexpr int attn_vstr(int D) { return D + 4; }
+constexpr int kAttnSpStr = kAttnChunk + 8;
 
 // Shared-memory carve-up of the chunk kernel for head size D and at most QN queries.
 struct AttnLayout {
-  size_t stage, q, kt, vt, sp, total;
+  size_t stage, q, kt, vt, sp, ef, total;
 };
 __host__ __device__ inline AttnLayout attn_layout(int D, int QN) {
   AttnLayout a;
-  a.stage = (size_t)2 * kAttnChunk * D * 4;         // ring entry 2s: K rows, 2s + 1: V rows
+  const size_t nmt = (size_t)(QN + 15) / 16;
+  a.stage = (size_t)kAttnChunk * (attn_kstr(D) + attn_vstr(D)) * 4;  // ring entry 2s: K rows, 2s + 1: V rows
   a.q = kAttnStages * a.stage;                       // query A fragments [m-tile][k-step][lane] (hi, lo)
-  a.kt = a.q + (size_t)((QN + 15) / 16) * (D / 16) * 32 * 32;  // tree K rows [16][D]
+  a.kt = a.q + nmt * (D / 16) * 32 * 32;             // tree K rows [16][D]
   a.vt = a.kt + (size_t)kMaxWidth * D * 4;           // tree V rows
-  a.sp = a.vt + (size_t)kMaxWidth * D * 4;           // scores [q][64]
-  a.total = a.sp + (size_t)QN * kAttnChunk * 4;
+  a.sp = a.vt + (size_t)kMaxWidth * D * 4;           // scores [q][kAttnSpStr]
+  a.ef = a.sp + (size_t)QN * kAttnSpStr * 4;         // weights e as A fragments [m-tile][slot step][lane] (hi, lo)
+  a.total = a.ef + nmt * (kAttnChunk / 16) * 32 * 32;
   return a;
 }
 
@@ -269,33 +278,51 @@ __device__ __forceinline__ void mma_split3(float (&d)[4], uint4 ahi, uint4 alo, 
 //           q = qh + ql, k = kh + kl: per 16-dimension step qh.kh + qh.kl + ql.kh, steps in order
 //           (the row of a score depends on its own query and key only);
 //   per chunk: m = max(M, max over visible slots), c = exp(M - m), e_j = exp(s_j - m),
-//           L = L * c + (butterfly sum of e over the 64 slots), O[d] = O[d] * c, then
-//           O[d] = fmaf(e_j, v_j[d], O[d]) over the visible slots in ascending order; M = m.
+//           L = L * c + (butterfly sum of e over the 64 slots, lane l holding slots 2l, 2l+1);
+//   values: the chunk sum P[d] = sum_j e_j v_j[d] on the tensor cores from the f16 splits
+//           e = eh + el, v = vh + vl: per 16-slot step eh.vh + eh.vl + el.vh, steps in order,
+//           then O[d] = fmaf(O[d], c, P[d]); M = m.
 // Slots below the committed length L read the cache; slots at L + e read the node's
-// ancestor at depth e (tree rows).  The last CTA of a KV head to finish (ticket) merges the
-// splits of every query in ascending order (M = max M_s, L = sum exp(M_s - M) L_s,
-// O = sum exp(M_s - M) O_s), writes O / L and the per-(node, head) maximum |O / L| that the
-// quantiser of the O projection reads (MERGE; otherwise k_attn_merge does the same merge with
-// one CTA per (node, head)).  Every order is a function of the logical position.
+// ancestor at depth e (tree rows); a 16-slot group reaching past the cache is multiplied
+// with each node's own rows (zero rows past the node), keeping that node's rows of the
+// result, so every row sees the same operations as in a step where those slots are cached.
+// The last CTA of a KV head to finish (ticket) merges the splits of every query in ascending
+// order (M = max M_s, L = sum exp(M_s - M) L_s, O = sum exp(M_s - M) O_s), writes O / L and
+// the per-(node, head) maximum |O / L| that the quantiser of the O projection reads (MERGE;
+// otherwise k_attn_merge does the same merge with one CTA per (node, head)).  Every order is
+// a function of the logical position.
+// (one CTA per SM: 168 registers keep the three warps of a sub-partition within its 16384)
 template <int D, int G, int QT, bool MERGE>
-__global__ void __launch_bounds__(kAttnThreads)
+__global__ void __maxnreg__(168)
     k_attn(SpecCtl* ctl, const TreeState* __restrict__ tree, int N, const float* __restrict__ qrot,
            const float* __restrict__ kc, const float* __restrict__ vc, int kv_cap, int Hq, int R,
            float* __restrict__ o_part, float2* __restrict__ ml_part, unsigned* __restrict__ tickets,
-           float* __restrict__ out, float2* __restrict__ mpart) {
+           float* __restrict__ out, float2* __restrict__ mpart, const __grid_constant__ CUtensorMap tm_k,
+           const __grid_constant__ CUtensorMap tm_v, int layer) {
   constexpr int CH = kAttnChunk;
-  constexpr int DL = D / 32;         // value dimensions per lane
+  constexpr int DL = D / 32;         // dimensions per lane in the merge
   constexpr int KS = D / 16;         // 16-dimension steps of a score
+  constexpr int VS = CH / 16;        // 16-slot steps of the value product
+  constexpr int NTW = D / 8 / kAttnWarps;  // 8-dimension n-tiles of the value product per warp
   constexpr int MT = (kMaxWidth * G + 15) / 16 < (QT + 1) / 2 ? (kMaxWidth * G + 15) / 16 : (QT + 1) / 2;
   constexpr int NE = 2 * kAttnStages;  // ring entries (K or V rows of one chunk)
+  constexpr int MSPAN = (16 % G == 0) ? 1 : 2;  // m-tiles that hold one node's rows, at most
+  constexpr int KSTR = attn_kstr(D), VSTR = attn_vstr(D), SPS = kAttnSpStr;
+  // scores of a fully cached chunk: WPM warps per m-tile, NTPW key n-tiles (8 keys) per warp
+  constexpr int WPM = kAttnWarps / MT, NTPW = (CH / 8) / WPM;
+  static_assert(CH / 8 == kAttnWarps, "one key n-tile per warp in chunks reaching past the cache");
+  static_assert((WPM & (WPM - 1)) == 0 && WPM * NTPW == CH / 8, "score partition");
   static_assert(D == 64 || D == 128, "head size");
+  static_assert(NTW >= 1 && NTW * 8 * kAttnWarps == D, "value n-tiles");
   // The committed length, the tree shape and the cached rows below it were written by
   // earlier steps, so the copies of the cached rows start before the dependency wait (the
   // kernel just before this one writes only the tree slots and the queries).
   griddep_launch();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_path[kMaxWidth][kMaxWidth];
-  __shared__ int s_dep[kMaxWidth];
+  __shared__ int s_dep[kMaxWidth], s_par[kMaxWidth];
+  __shared__ float s_cs[kMaxWidth * 8];  // per-query rescale c of the running values (this chunk)
+  __shared__ float s_M[kMaxWidth * 8], s_L[kMaxWidth * 8];  // running max and sum per query
   __shared__ uint64_t full[NE], empty[NE];
   __shared__ unsigned s_last;
   const int kh = blockIdx.y;
@@ -307,15 +334,21 @@ __global__ void __launch_bounds__(kAttnThreads)
   if (c_begin >= nch) return;  // uniform over the CTA
   const int nsa = (nch + R - 1) / R;  // CTAs of this head that hold chunks
   const int QN = N * G;
+  const int nmt = (QN + 15) / 16;
   const AttnLayout lay = attn_layout(D, QN);
   uint8_t* Qf = smem + lay.q;
   float* Kt = reinterpret_cast<float*>(smem + lay.kt);
   float* Vt = reinterpret_cast<float*>(smem + lay.vt);
   float* SP = reinterpret_cast<float*>(smem + lay.sp);
+  uint32_t* EF = reinterpret_cast<uint32_t*>(smem + lay.ef);
   const float* kb = kc + (size_t)kh * kv_cap * D;
   const float* vb = vc + (size_t)kh * kv_cap * D;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t half = lay.stage / 2;  // bytes of one ring entry
+  const int lg = lane >> 2, lt = lane & 3;  // fragment row group and thread-in-group
+  // ring entry e: K rows of stage e / 2 (even e) or its V rows (odd e)
+  auto ring_entry = [&](int e) -> uint8_t* {
+    return smem + (size_t)(e >> 1) * lay.stage + ((e & 1) ? (size_t)CH * KSTR * 4 : 0);
+  };
   if (threadIdx.x == 0) {
     for (int i = 0; i < NE; ++i) {
       mbar_init(&full[i], 1);
@@ -327,12 +360,14 @@ __global__ void __launch_bounds__(kAttnThreads)
   __syncthreads();
 
   if (warp == kAttnWarps) {
-    // ---------------- copy warp: entries K(c0) V(c0) K(c1) V(c1) ... ----------------
+    // ---------------- copy warp: entries K(c0) V(c0) K(c1) V(c1) ..., one TMA box of 64 rows
+    // each (rows land at the padded strides; columns past D and rows past the cache read zero;
+    // rows between L and the chunk end are never read from the ring)
     if (lane == 0) {
       int n = 0;  // entries issued
       for (int c = c_begin; c < c_end; ++c) {
         const int P0 = c * CH;
-        const int ncache = max(0, min(CH, L - P0));
+        const bool any = L > P0;  // the chunk holds cached rows
         for (int kv = 0; kv < 2; ++kv, ++n) {
           const int e = n % NE;
           if (n >= NE && !mbar_wait(&empty[e], ((n / NE) - 1) & 1)) {
@@ -340,10 +375,8 @@ __global__ void __launch_bounds__(kAttnThreads)
             c = c_end;
             break;
           }
-          mbar_expect_tx(&full[e], (unsigned)(ncache * D * 4));
-          if (ncache > 0)
-            bulk_g2s(smem + (size_t)e * half, (kv ? vb : kb) + (size_t)P0 * D, (unsigned)(ncache * D * 4),
-                     &full[e]);
+          mbar_expect_tx(&full[e], any ? (unsigned)(CH * (kv ? VSTR : KSTR) * 4) : 0u);
+          if (any) tma_load_4d(ring_entry(e), kv ? &tm_v : &tm_k, 0, P0, kh, layer, &full[e]);
         }
       }
       // every issued copy lands before the CTA exits
@@ -356,6 +389,28 @@ __global__ void __launch_bounds__(kAttnThreads)
     return;
   }
 
+  // ---------------- compute warps ----------------
+  // Set-up that needs only earlier steps' state (the tree shape) or nothing, before the
+  // dependency wait: node depths and root paths, zeroed weight fragments (rows past QN stay
+  // zero: their products are discarded), the running max and sum.
+  if (threadIdx.x < N) {
+    s_dep[threadIdx.x] = tree->depth[threadIdx.x];
+    s_par[threadIdx.x] = tree->parent[threadIdx.x];
+  }
+  for (int idx = threadIdx.x; idx < nmt * VS * 32 * 8; idx += 32 * kAttnWarps) EF[idx] = 0u;
+  for (int q = threadIdx.x; q < QN; q += 32 * kAttnWarps) {
+    s_M[q] = -INFINITY;
+    s_L[q] = 0.0f;
+  }
+  consumers_sync();
+  if (threadIdx.x < N) {
+    const int i = threadIdx.x;
+    int cur = i;
+    for (int e = s_dep[i]; e >= 0; --e) {
+      s_path[i][e] = cur;
+      cur = e > 0 ? s_par[cur] : 0;
+    }
+  }
   griddep_wait();
   if (!consumers_all(!stopped(ctl))) {
     // keep the ring consistent for the copy warp: consume every entry it issues
@@ -370,65 +425,75 @@ __global__ void __launch_bounds__(kAttnThreads)
       }
     return;
   }
-  // ---------------- compute warps ----------------
-  if (threadIdx.x < N) {
-    const int i = threadIdx.x;
-    const int d = tree->depth[i];
-    s_dep[i] = d;
-    int cur = i;
-    for (int e = d; e >= 0; --e) {
-      s_path[i][e] = cur;
-      cur = e > 0 ? tree->parent[cur] : 0;
-    }
-  }
   // queries of the KV head (the G heads of kh are consecutive in qrot) and the tree rows
-  // (slots L .. L+N-1, read by the chunks that reach past L)
+  // (slots L .. L+N-1, read by the chunks that reach past L), both written by the kernel
+  // just before this one; every load is issued before the first split.
   // A fragments of m16n8k16 (rows = queries, columns = dimensions), split into f16 hi and lo:
   // lane (g, t) of m-tile mt, step s holds rows g, g+8 and columns 2t, 2t+1, 2t+8, 2t+9
   {
-    const int nmt = (QN + 15) / 16;
-    for (int idx = threadIdx.x; idx < nmt * KS * 32; idx += 32 * kAttnWarps) {
+    constexpr int QI = (MT * KS * 32 + 32 * kAttnWarps - 1) / (32 * kAttnWarps);
+    float v[QI][8];
+#pragma unroll
+    for (int it = 0; it < QI; ++it) {
+      const int idx = threadIdx.x + it * 32 * kAttnWarps;
       const int ln = idx & 31, st = (idx >> 5) % KS, mt = (idx >> 5) / KS;
       const int g = ln >> 2, t = ln & 3;
-      float v[8];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int q = mt * 16 + g + 8 * h;
-        if (q < QN) {
+        float2 lo2 = make_float2(0.0f, 0.0f), hi2 = make_float2(0.0f, 0.0f);
+        if (idx < nmt * KS * 32 && q < QN) {
           const float* qr = qrot + ((size_t)(q / G) * Hq + kh * G + q % G) * D + st * 16 + 2 * t;
-          const float2 lo2 = *reinterpret_cast<const float2*>(qr);
-          const float2 hi2 = *reinterpret_cast<const float2*>(qr + 8);
-          v[2 * h] = lo2.x; v[2 * h + 1] = lo2.y; v[4 + 2 * h] = hi2.x; v[5 + 2 * h] = hi2.y;
-        } else {
-          v[2 * h] = v[2 * h + 1] = v[4 + 2 * h] = v[5 + 2 * h] = 0.0f;
+          lo2 = *reinterpret_cast<const float2*>(qr);
+          hi2 = *reinterpret_cast<const float2*>(qr + 8);
         }
+        v[it][2 * h] = lo2.x; v[it][2 * h + 1] = lo2.y; v[it][4 + 2 * h] = hi2.x; v[it][5 + 2 * h] = hi2.y;
       }
+    }
+    constexpr int TI = (kMaxWidth * D / 4 + 32 * kAttnWarps - 1) / (32 * kAttnWarps);
+    float4 kt[TI], vt[TI];
+#pragma unroll
+    for (int it = 0; it < TI; ++it) {
+      const int idx = threadIdx.x + it * 32 * kAttnWarps;
+      if (idx < N * D / 4) {
+        kt[it] = reinterpret_cast<const float4*>(kb + (size_t)L * D)[idx];
+        vt[it] = reinterpret_cast<const float4*>(vb + (size_t)L * D)[idx];
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < QI; ++it) {
+      const int idx = threadIdx.x + it * 32 * kAttnWarps;
+      if (idx >= nmt * KS * 32) continue;
+      const int ln = idx & 31, st = (idx >> 5) % KS, mt = (idx >> 5) / KS;
       uint4 ah, al;  // registers a0 (row g), a1 (row g+8), a2 (row g, +8 columns), a3 (row g+8, +8)
-      split_h2(v[0], v[1], ah.x, al.x);
-      split_h2(v[2], v[3], ah.y, al.y);
-      split_h2(v[4], v[5], ah.z, al.z);
-      split_h2(v[6], v[7], ah.w, al.w);
+      split_h2(v[it][0], v[it][1], ah.x, al.x);
+      split_h2(v[it][2], v[it][3], ah.y, al.y);
+      split_h2(v[it][4], v[it][5], ah.z, al.z);
+      split_h2(v[it][6], v[it][7], ah.w, al.w);
       uint4* dst = reinterpret_cast<uint4*>(Qf + ((size_t)(mt * KS + st) * 32 + ln) * 32);
       dst[0] = ah;
       dst[1] = al;
     }
-  }
-  for (int idx = threadIdx.x; idx < N * D / 4; idx += 32 * kAttnWarps) {
-    reinterpret_cast<float4*>(Kt)[idx] = reinterpret_cast<const float4*>(kb + (size_t)L * D)[idx];
-    reinterpret_cast<float4*>(Vt)[idx] = reinterpret_cast<const float4*>(vb + (size_t)L * D)[idx];
+#pragma unroll
+    for (int it = 0; it < TI; ++it) {
+      const int idx = threadIdx.x + it * 32 * kAttnWarps;
+      if (idx < N * D / 4) {
+        reinterpret_cast<float4*>(Kt)[idx] = kt[it];
+        reinterpret_cast<float4*>(Vt)[idx] = vt[it];
+      }
+    }
   }
   consumers_sync();
 
-  // running state of the queries w + 8u of this warp
-  float Mr[QT], Lr[QT], Or[QT][DL];
+  // values in the layout of the value product (warp w owns the dimension n-tiles
+  // w*NTW .. w*NTW + NTW-1 of every query)
+  float Or[MT][NTW][4];
 #pragma unroll
-  for (int u = 0; u < QT; ++u) {
-    Mr[u] = -INFINITY;
-    Lr[u] = 0.0f;
+  for (int m = 0; m < MT; ++m)
 #pragma unroll
-    for (int d = 0; d < DL; ++d) Or[u][d] = 0.0f;
-  }
-  const int d0 = lane * DL;
+    for (int nn = 0; nn < NTW; ++nn)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) Or[m][nn][e] = 0.0f;
   bool ok = true;
   int n = 0;  // ring entries consumed
   for (int c = c_begin; c < c_end; ++c, n += 2) {
@@ -438,30 +503,59 @@ __global__ void __launch_bounds__(kAttnThreads)
       ok = false;  // a bounded wait expired: stop computing (uniform over the compute warps)
       break;
     }
-    const float* Ks = reinterpret_cast<const float*>(smem + (size_t)eK * half);
-    const float* Vs = reinterpret_cast<const float*>(smem + (size_t)eV * half);
+    const float* Ks = reinterpret_cast<const float*>(ring_entry(eK));
+    const float* Vs = reinterpret_cast<const float*>(ring_entry(eV));
     const int P0 = c * CH;
     const int jc = min(CH, L - P0);  // slots below jc come from the cache
 
-    // ---- scores on the tensor cores: warp w takes keys 8w..8w+7 (one n-tile) for every m-tile
-    // of queries; a score is the sum over 16-dimension steps of hi*hi + hi*lo + lo*hi of the
-    // f16 splits of the query and the key, accumulated in f32 in that fixed order.
+    // ---- scores on the tensor cores: a score is the sum over 16-dimension steps of hi*hi +
+    // hi*lo + lo*hi of the f16 splits of the query and the key, accumulated in f32 in that
+    // fixed order (whichever warp computes it).
     {
-      const int g = lane >> 2, t = lane & 3;
-      const int nmt = (QN + 15) / 16;
-      const int j = 8 * warp + g;  // key of this lane's B fragment
-      auto store = [&](const float (&acc)[4], int mt, int node) {
-        // node < 0: every row; else only the rows of that node
+      auto store = [&](const float (&acc)[4], int mt, int nt, int node) {
+        // node < 0: every row; else only the rows of that node; keys 8nt + 2t, +1 as one float2
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int q = mt * 16 + g + ((e & 2) ? 8 : 0);
-          const int key = 8 * warp + 2 * t + (e & 1);
+        for (int h = 0; h < 2; ++h) {
+          const int q = mt * 16 + lg + 8 * h;
           if (q >= QN || (node >= 0 && q / G != node)) continue;
-          const int p = P0 + key;
-          SP[(size_t)q * CH + key] = (p <= L + s_dep[q / G]) ? acc[e] : -INFINITY;
+          const int key = 8 * nt + 2 * lt;
+          const int lim = L + s_dep[q / G] - P0;  // last slot of this chunk the query sees
+          *reinterpret_cast<float2*>(SP + (size_t)q * SPS + key) =
+              make_float2(key <= lim ? acc[2 * h] : -INFINITY, key + 1 <= lim ? acc[2 * h + 1] : -INFINITY);
         }
       };
-      if (8 * warp + 7 < jc) {  // every key of the n-tile is cached: one B for all queries
+      if (jc >= CH) {
+        // every key of the chunk is cached: warp w takes m-tile w / WPM and the NTPW key n-tiles
+        // from (w % WPM) * NTPW, one B per n-tile for all queries of the m-tile
+        const int mw = warp / WPM, nt0 = (warp % WPM) * NTPW;
+        if (mw < nmt) {
+          float acc[NTPW][4];
+#pragma unroll
+          for (int i = 0; i < NTPW; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[i][e] = 0.0f;
+#pragma unroll
+          for (int st = 0; st < KS; ++st) {
+            const uint4* af = reinterpret_cast<const uint4*>(Qf + ((size_t)(mw * KS + st) * 32 + lane) * 32);
+            const uint4 ah = af[0], al = af[1];
+#pragma unroll
+            for (int i = 0; i < NTPW; ++i) {
+              const float* kr = Ks + (size_t)(8 * (nt0 + i) + lg) * KSTR + st * 16 + 2 * lt;
+              const float2 k0 = *reinterpret_cast<const float2*>(kr);
+              const float2 k1 = *reinterpret_cast<const float2*>(kr + 8);
+              uint32_t bh0, bl0, bh1, bl1;
+              split_h2(k0.x, k0.y, bh0, bl0);
+              split_h2(k1.x, k1.y, bh1, bl1);
+              mma_split3(acc[i], ah, al, bh0, bh1, bl0, bl1);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < NTPW; ++i) store(acc[i], mw, nt0 + i, -1);
+        }
+      } else if (8 * warp + 7 < jc) {
+        // chunk reaching past the cache, warp w takes key n-tile w for every m-tile; every key
+        // of this n-tile is cached: one B for all queries
+        const int j = 8 * warp + lg;  // key of this lane's B fragment
         float acc[MT][4];
 #pragma unroll
         for (int m = 0; m < MT; ++m)
@@ -469,7 +563,7 @@ __global__ void __launch_bounds__(kAttnThreads)
           for (int e = 0; e < 4; ++e) acc[m][e] = 0.0f;
 #pragma unroll
         for (int st = 0; st < KS; ++st) {
-          const float* kr = Ks + (size_t)j * D + st * 16 + 2 * t;
+          const float* kr = Ks + (size_t)j * KSTR + st * 16 + 2 * lt;
           const float2 k0 = *reinterpret_cast<const float2*>(kr);
           const float2 k1 = *reinterpret_cast<const float2*>(kr + 8);
           uint32_t bh0, bl0, bh1, bl1;
@@ -484,33 +578,63 @@ __global__ void __launch_bounds__(kAttnThreads)
         }
 #pragma unroll
         for (int m = 0; m < MT; ++m)
-          if (m < nmt) store(acc[m], m, -1);
+          if (m < nmt) store(acc[m], m, warp, -1);
       } else {
-        // n-tile reaching past the cache: keys at L + e are each node's ancestors, so every
-        // node takes its own B (cached keys are the same rows for all nodes)
+        // n-tile w reaching past the cache: keys at L + e are each node's ancestors, so every
+        // node takes its own B (cached keys are the same rows for all nodes); four nodes at a
+        // time, each over the (at most MSPAN) m-tiles that hold its rows
+        const int j = 8 * warp + lg;
         const int p = P0 + j;
-        for (int node = 0; node < N; ++node) {
-          const float* kr = nullptr;
-          if (j < jc) kr = Ks + (size_t)j * D;
-          else if (p - L <= s_dep[node]) kr = Kt + (size_t)s_path[node][p - L] * D;
-          const int m_lo = (node * G) / 16, m_hi = (node * G + G - 1) / 16;
-          for (int m = m_lo; m <= m_hi; ++m) {
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int nb = 0; nb < N; nb += 4) {
+          const float* kr[4];
+          int mlo[4], mcnt[4];  // first m-tile and m-tile count of each node (0: no node)
 #pragma unroll
-            for (int st = 0; st < KS; ++st) {
+          for (int k = 0; k < 4; ++k) {
+            const int node = nb + k;
+            kr[k] = nullptr;
+            mlo[k] = 0;
+            mcnt[k] = 0;
+            if (node < N) {
+              if (j < jc) kr[k] = Ks + (size_t)j * KSTR;
+              else if (p - L <= s_dep[node]) kr[k] = Kt + (size_t)s_path[node][p - L] * D;
+              mlo[k] = (node * G) / 16;
+              mcnt[k] = (node * G + G - 1) / 16 - mlo[k] + 1;
+            }
+          }
+          float acc[4][MSPAN][4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int mi = 0; mi < MSPAN; ++mi)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[k][mi][e] = 0.0f;
+#pragma unroll
+          for (int st = 0; st < KS; ++st) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              if (mcnt[k] == 0) continue;
               float2 k0 = make_float2(0.0f, 0.0f), k1 = make_float2(0.0f, 0.0f);
-              if (kr != nullptr) {
-                k0 = *reinterpret_cast<const float2*>(kr + st * 16 + 2 * t);
-                k1 = *reinterpret_cast<const float2*>(kr + st * 16 + 2 * t + 8);
+              if (kr[k] != nullptr) {
+                k0 = *reinterpret_cast<const float2*>(kr[k] + st * 16 + 2 * lt);
+                k1 = *reinterpret_cast<const float2*>(kr[k] + st * 16 + 2 * lt + 8);
               }
               uint32_t bh0, bl0, bh1, bl1;
               split_h2(k0.x, k0.y, bh0, bl0);
               split_h2(k1.x, k1.y, bh1, bl1);
-              const uint4* af = reinterpret_cast<const uint4*>(Qf + ((size_t)(m * KS + st) * 32 + lane) * 32);
-              mma_split3(acc, af[0], af[1], bh0, bh1, bl0, bl1);
+#pragma unroll
+              for (int mi = 0; mi < MSPAN; ++mi) {
+                if (mi >= mcnt[k]) continue;
+                const uint4* af =
+                    reinterpret_cast<const uint4*>(Qf + ((size_t)((mlo[k] + mi) * KS + st) * 32 + lane) * 32);
+                mma_split3(acc[k][mi], af[0], af[1], bh0, bh1, bl0, bl1);
+              }
             }
-            store(acc, m, node);
           }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int mi = 0; mi < MSPAN; ++mi)
+              if (mi < mcnt[k]) store(acc[k][mi], mlo[k] + mi, warp, nb + k);
         }
       }
     }
@@ -522,164 +646,192 @@ __global__ void __launch_bounds__(kAttnThreads)
       break;
     }
 
-    // ---- running statistics and values: warp w, queries w + 8u
+    // ---- running statistics: warp w, queries w + 8u (interleaved); lane l holds slots 2l,
+    // 2l+1.  The weights e go to the A fragments of the value product (f16 hi and lo): slot
+    // pair (2l, 2l+1) is register (l & 4 ? 2 : 0) + (row >= 8) of fragment lane
+    // 4 * (row & 7) + (l & 3), step l / 8, m-tile q / 16 (rows q and q + 8 of an m-tile
+    // belong to the same warp).
     {
-      float e0[QT], e1[QT];
-      int last[QT];
-      int lmin = CH, lmax = -1;
+      float2 sv[QT];
+      float mq[QT], mx[QT], l[QT], cs[QT], e0[QT], e1[QT];
+      bool act[QT];
 #pragma unroll
       for (int u = 0; u < QT; ++u) {
         const int q = warp + kAttnWarps * u;
-        last[u] = -1;
-        e0[u] = e1[u] = 0.0f;
-        if (q < QN) {
-          last[u] = min(CH - 1, L + s_dep[q / G] - P0);
-          if (last[u] >= 0) {
-            const float* sq = SP + (size_t)q * CH;
-            const float s0 = sq[lane], s1 = sq[lane + 32];
-            const float m = fmaxf(Mr[u], warp_max(fmaxf(s0, s1)));
-            const float cs = (Mr[u] == -INFINITY) ? 0.0f : expf(Mr[u] - m);
-            e0[u] = (s0 == -INFINITY) ? 0.0f : expf(s0 - m);
-            e1[u] = (s1 == -INFINITY) ? 0.0f : expf(s1 - m);
-            float l = e0[u] + e1[u];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-            Lr[u] = fmaf(Lr[u], cs, l);
-            Mr[u] = m;
-#pragma unroll
-            for (int d = 0; d < DL; ++d) Or[u][d] = Or[u][d] * cs;
-            lmin = min(lmin, last[u]);
-          }
-          // the row now holds the weights e (zero for a chunk beyond the node)
-          SP[(size_t)q * CH + lane] = e0[u];
-          SP[(size_t)q * CH + lane + 32] = e1[u];
+        act[u] = q < QN && L + s_dep[min(q, QN - 1) / G] - P0 >= 0;  // the query sees this chunk
+        sv[u] = make_float2(-INFINITY, -INFINITY);
+        mq[u] = -INFINITY;
+        if (act[u]) {
+          sv[u] = *reinterpret_cast<const float2*>(SP + (size_t)q * SPS + 2 * lane);
+          mq[u] = s_M[q];
         }
-        lmax = max(lmax, last[u]);
+        mx[u] = fmaxf(sv[u].x, sv[u].y);
       }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int u = 0; u < QT; ++u) mx[u] = fmaxf(mx[u], __shfl_xor_sync(0xffffffffu, mx[u], off));
+#pragma unroll
+      for (int u = 0; u < QT; ++u) {
+        const float m = fmaxf(mq[u], mx[u]);
+        mx[u] = m;
+        cs[u] = 1.0f;
+        e0[u] = e1[u] = 0.0f;
+        if (act[u]) {
+          cs[u] = (mq[u] == -INFINITY) ? 0.0f : expf(mq[u] - m);
+          e0[u] = (sv[u].x == -INFINITY) ? 0.0f : expf(sv[u].x - m);
+          e1[u] = (sv[u].y == -INFINITY) ? 0.0f : expf(sv[u].y - m);
+        }
+        l[u] = e0[u] + e1[u];
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int u = 0; u < QT; ++u) l[u] += __shfl_xor_sync(0xffffffffu, l[u], off);
       __syncwarp();
-      // slots every active query sees, from the cache: no per-query tests (an inactive
-      // query has e = 0 and its state is not stored); four slots per step
-      const int jall = min(min(lmin + 1, jc), lmax + 1);
-      int j = 0;
-      if (jall == CH) {
-        // whole cached chunk: constant trip count, weights read four at a time (broadcast)
 #pragma unroll
-        for (int jj = 0; jj < CH; jj += 4) {
-          float v[4][DL];
+      for (int u = 0; u < QT; ++u) {
+        const int q = warp + kAttnWarps * u;
+        if (q >= QN) break;
+        if (lane == 0) {
+          if (act[u]) {
+            s_L[q] = fmaf(s_L[q], cs[u], l[u]);
+            s_M[q] = mx[u];
+          }
+          s_cs[q] = cs[u];
+        }
+        // the fragments hold 2^15 e (exact), so that small weights keep their low part in the
+        // normal f16 range; the running values carry the same factor until they are stored
+        uint32_t eh, el;
+        split_h2(e0[u] * kAttnEScale, e1[u] * kAttnEScale, eh, el);
+        const int r = q & 15;
+        uint32_t* f = EF + ((size_t)((q >> 4) * VS + (lane >> 3)) * 32 + 4 * (r & 7) + (lane & 3)) * 8 +
+                      ((lane & 4) ? 2 : 0) + (r >> 3);
+        f[0] = eh;
+        f[4] = el;
+      }
+    }
+    consumers_sync();
+
+    // ---- values on the tensor cores: O = O * c, then O += e . V for this warp's n-tiles,
+    // 16-slot steps in order (rows past QN are never stored)
+    {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            if (DL == 4) {
-              const float4 t = *reinterpret_cast<const float4*>(Vs + (size_t)(jj + k) * D + d0);
-              v[k][0] = t.x; v[k][1 % DL] = t.y; v[k][2 % DL] = t.z; v[k][3 % DL] = t.w;
-            } else {
-              const float2 t = *reinterpret_cast<const float2*>(Vs + (size_t)(jj + k) * D + d0);
-              v[k][0] = t.x; v[k][1 % DL] = t.y;
+      for (int m = 0; m < MT; ++m) {
+        if (m >= nmt) break;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float cq = s_cs[min(m * 16 + lg + ((e & 2) ? 8 : 0), QN - 1)];
+#pragma unroll
+          for (int nn = 0; nn < NTW; ++nn) Or[m][nn][e] *= cq;
+        }
+      }
+      // B fragment of n-tile nn from slot rows r0..r3 (slots 2t, 2t+1, 2t+8, 2t+9 of the step);
+      // a null row reads as zero
+      auto vfrag = [&](const float* r0, const float* r1, const float* r2, const float* r3, int nn,
+                       uint32_t& bh0, uint32_t& bl0, uint32_t& bh1, uint32_t& bl1) {
+        const int dcol = (warp * NTW + nn) * 8 + lg;
+        const float x0 = r0 ? r0[dcol] : 0.0f, x1 = r1 ? r1[dcol] : 0.0f;
+        const float x2 = r2 ? r2[dcol] : 0.0f, x3 = r3 ? r3[dcol] : 0.0f;
+        split_h2(x0, x1, bh0, bl0);
+        split_h2(x2, x3, bh1, bl1);
+      };
+      // steps past the last slot that any node sees add nothing (their weights are zero); the
+      // leading steps whose 16 slots are all cached take one B for all queries
+      const int nst = min(CH - 1, L + maxd - P0) / 16 + 1;
+      const int ncs = min(nst, max(jc, 0) / 16);
+#pragma unroll
+      for (int st = 0; st < VS; ++st) {
+        if (st < ncs) {
+          const int js = st * 16 + 2 * lt;  // slots js, js+1, js+8, js+9 of this lane's B
+          uint32_t bh0[NTW], bl0[NTW], bh1[NTW], bl1[NTW];
+          const float* r0 = Vs + (size_t)js * VSTR;
+#pragma unroll
+          for (int nn = 0; nn < NTW; ++nn)
+            vfrag(r0, r0 + VSTR, r0 + 8 * VSTR, r0 + 9 * VSTR, nn, bh0[nn], bl0[nn], bh1[nn], bl1[nn]);
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            if (m >= nmt) break;
+            const uint4* af = reinterpret_cast<const uint4*>(EF + ((size_t)(m * VS + st) * 32 + lane) * 8);
+            const uint4 ah = af[0], al = af[1];
+#pragma unroll
+            for (int nn = 0; nn < NTW; ++nn) mma_split3(Or[m][nn], ah, al, bh0[nn], bh1[nn], bl0[nn], bl1[nn]);
+          }
+        }
+      }
+      for (int st = ncs; st < nst; ++st) {
+        const int js = st * 16 + 2 * lt;
+        {
+          // per node: its own rows for the slots of this step (cache below jc, ancestors from
+          // L on, zero past the node); four nodes at a time
+          auto vrow = [&](int node, int kk) -> const float* {
+            const int jj = js + (kk & 1) + ((kk & 2) ? 8 : 0);
+            const int p = P0 + jj;
+            if (jj < jc) return Vs + (size_t)jj * VSTR;
+            if (p - L <= s_dep[node]) return Vt + (size_t)s_path[node][p - L] * D;
+            return nullptr;
+          };
+          for (int nb = 0; nb < N; nb += 4) {
+            const int nlast = min(N, nb + 4) - 1;
+            const int glo = (nb * G) / 16, ghi = (nlast * G + G - 1) / 16;  // m-tiles of the group
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              if (m >= nmt) break;
+              if (m < glo || m > ghi) continue;
+              const uint4* af = reinterpret_cast<const uint4*>(EF + ((size_t)(m * VS + st) * 32 + lane) * 8);
+              const uint4 ah = af[0], al = af[1];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int node = nb + k;
+                if (node > nlast || m < (node * G) / 16 || m > (node * G + G - 1) / 16) continue;
+                const float* r0 = vrow(node, 0);
+                const float* r1 = vrow(node, 1);
+                const float* r2 = vrow(node, 2);
+                const float* r3 = vrow(node, 3);
+#pragma unroll
+                for (int nn = 0; nn < NTW; ++nn) {
+                  uint32_t bh0, bl0, bh1, bl1;
+                  vfrag(r0, r1, r2, r3, nn, bh0, bl0, bh1, bl1);
+                  float d[4] = {Or[m][nn][0], Or[m][nn][1], Or[m][nn][2], Or[m][nn][3]};
+                  mma_split3(d, ah, al, bh0, bh1, bl0, bl1);
+                  // keep the rows of this node (the other rows take their own node's rows)
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const int q = m * 16 + lg + ((e & 2) ? 8 : 0);
+                    if (q < QN && q / G == node) Or[m][nn][e] = d[e];
+                  }
+                }
+              }
             }
           }
-#pragma unroll
-          for (int u = 0; u < QT; ++u) {
-            const int q = min(warp + kAttnWarps * u, QN - 1);  // an inactive query's sums are discarded
-            const float4 e4 = *reinterpret_cast<const float4*>(SP + (size_t)q * CH + jj);
-            const float e[4] = {e4.x, e4.y, e4.z, e4.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-#pragma unroll
-              for (int d = 0; d < DL; ++d) Or[u][d] = fmaf(e[k], v[k][d], Or[u][d]);
-          }
-        }
-        j = CH;
-      }
-      auto vrow = [&](int jj, float (&v)[DL]) {
-        if (DL == 4) {
-          const float4 t = *reinterpret_cast<const float4*>(Vs + (size_t)jj * D + d0);
-          v[0] = t.x; v[1 % DL] = t.y; v[2 % DL] = t.z; v[3 % DL] = t.w;
-        } else {
-          const float2 t = *reinterpret_cast<const float2*>(Vs + (size_t)jj * D + d0);
-          v[0] = t.x; v[1 % DL] = t.y;
-        }
-      };
-      for (; j + 4 <= min(jall, 32); j += 4) {
-        float v[4][DL];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) vrow(j + k, v[k]);
-#pragma unroll
-        for (int u = 0; u < QT; ++u) {
-          float e[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) e[k] = __shfl_sync(0xffffffffu, e0[u], j + k);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int d = 0; d < DL; ++d) Or[u][d] = fmaf(e[k], v[k][d], Or[u][d]);
-        }
-      }
-      for (; j < min(jall, 32); ++j) {
-        float v[DL];
-        vrow(j, v);
-#pragma unroll
-        for (int u = 0; u < QT; ++u) {
-          const float e = __shfl_sync(0xffffffffu, e0[u], j);
-#pragma unroll
-          for (int d = 0; d < DL; ++d) Or[u][d] = fmaf(e, v[d], Or[u][d]);
-        }
-      }
-      for (; j + 4 <= jall; j += 4) {
-        float v[4][DL];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) vrow(j + k, v[k]);
-#pragma unroll
-        for (int u = 0; u < QT; ++u) {
-          float e[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) e[k] = __shfl_sync(0xffffffffu, e1[u], j + k - 32);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int d = 0; d < DL; ++d) Or[u][d] = fmaf(e[k], v[k][d], Or[u][d]);
-        }
-      }
-      for (; j < jall; ++j) {
-        float v[DL];
-        vrow(j, v);
-#pragma unroll
-        for (int u = 0; u < QT; ++u) {
-          const float e = __shfl_sync(0xffffffffu, e1[u], j - 32);
-#pragma unroll
-          for (int d = 0; d < DL; ++d) Or[u][d] = fmaf(e, v[d], Or[u][d]);
-        }
-      }
-      // remaining slots: per query (warp-uniform tests), cache or tree rows
-      for (; j <= lmax; ++j) {
-        const int p = P0 + j;
-#pragma unroll
-        for (int u = 0; u < QT; ++u) {
-          const float e = __shfl_sync(0xffffffffu, j < 32 ? e0[u] : e1[u], j & 31);
-          if (j > last[u]) continue;
-          const int q = warp + kAttnWarps * u;
-          const float* vr = p < L ? Vs + (size_t)j * D : Vt + (size_t)s_path[q / G][p - L] * D;
-#pragma unroll
-          for (int d = 0; d < DL; ++d) Or[u][d] = fmaf(e, vr[d0 + d], Or[u][d]);
         }
       }
     }
     consumers_sync();
     if (threadIdx.x == 0) mbar_arrive(&empty[eV]);
   }
-
   // ---- this split's partial, then the merge by the last split of the head
   if (ok) {
 #pragma unroll
     for (int u = 0; u < QT; ++u) {
       const int q = warp + kAttnWarps * u;
-      if (q >= QN || L + s_dep[q / G] < c_begin * CH) continue;
-      const int i = q / G, g = q % G;
-      const size_t ob = ((size_t)blockIdx.x * kMaxWidth + i) * Hq + kh * G + g;
-      float* dst = o_part + ob * D + d0;
-      if (DL == 4)
-        *reinterpret_cast<float4*>(dst) = make_float4(Or[u][0], Or[u][1 % DL], Or[u][2 % DL], Or[u][3 % DL]);
-      else
-        *reinterpret_cast<float2*>(dst) = make_float2(Or[u][0], Or[u][1 % DL]);
-      if (lane == 0) ml_part[ob] = make_float2(Mr[u], Lr[u]);
+      if (q >= QN) break;
+      if (L + s_dep[q / G] < c_begin * CH) continue;
+      if (lane == 0) ml_part[((size_t)blockIdx.x * kMaxWidth + q / G) * Hq + kh * G + q % G] = make_float2(s_M[q], s_L[q]);
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      if (m >= nmt) break;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int q = m * 16 + lg + 8 * h;
+        if (q >= QN || L + s_dep[q / G] < c_begin * CH) continue;
+        const size_t ob = ((size_t)blockIdx.x * kMaxWidth + q / G) * Hq + kh * G + q % G;
+#pragma unroll
+        for (int nn = 0; nn < NTW; ++nn)
+          *reinterpret_cast<float2*>(o_part + ob * D + (warp * NTW + nn) * 8 + 2 * lt) =
+              make_float2(Or[m][nn][2 * h] * (1.0f / kAttnEScale), Or[m][nn][2 * h + 1] * (1.0f / kAttnEScale));
+      }
     }
   }
   if (!MERGE) return;
@@ -696,6 +848,7 @@ __global__ void __launch_bounds__(kAttnThreads)
   }
   consumers_sync();
   if (!s_last) return;
+  const int d0 = lane * DL;  // merge: lane owns DL consecutive dimensions
   for (int q = warp; q < QN; q += kAttnWarps) {
     const int i = q / G, g = q % G;
     const int smax = ((L + s_dep[i]) / CH) / R;  // splits that saw this node
@@ -900,7 +1053,8 @@ cudaError_t attn_launch(bool configure, size_t smem, const DecoderBufs& b, const
   const int R = (b.n_chunks + splits - 1) / splits;  // chunks per split (fixed per session)
   cudaError_t e = launch_pdl(k_attn<D, G, QT, MERGE>, dim3(splits, m.Hkv), dim3(kAttnThreads),
                              attn_smem_bytes(D, N * G), st, b.ctl, (const TreeState*)b.tree, N, (const float*)b.qrot,
-                             kc, vc, b.kv_cap, m.Hq, R, b.o_part, (float2*)b.ml_part, b.attn_tickets, b.qkv, b.qpart);
+                             kc, vc, b.kv_cap, m.Hq, R, b.o_part, (float2*)b.ml_part, b.attn_tickets, b.qkv, b.qpart,
+                             b.tm_k, b.tm_v, layer);
   if (e != cudaSuccess || MERGE) return e;
   return launch_pdl(k_attn_merge, dim3(N, m.Hq), dim3(m.D), 0, st, (const SpecCtl*)b.ctl, (const TreeState*)b.tree,
                     (const float*)b.o_part, (const float2*)b.ml_part, m.Hq, m.D, R, b.qkv, b.qpart);
@@ -947,6 +1101,30 @@ cudaError_t attn_any(int D, int G, bool configure, size_t smem, const DecoderBuf
 }
 }  // namespace
 
+cudaError_t attn_tensor_maps(DecoderBufs& b, const ModelDims& m) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess) return e;
+  if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+  const Encode encode = reinterpret_cast<Encode>(fn);
+  const cuuint64_t dims[4] = {(cuuint64_t)m.D, (cuuint64_t)b.kv_cap, (cuuint64_t)m.Hkv, (cuuint64_t)m.n_layers};
+  const cuuint64_t strides[3] = {(cuuint64_t)m.D * 4, (cuuint64_t)b.kv_cap * m.D * 4,
+                                 (cuuint64_t)m.Hkv * b.kv_cap * m.D * 4};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  for (int kv = 0; kv < 2; ++kv) {
+    const cuuint32_t box[4] = {(cuuint32_t)(kv ? attn_vstr(m.D) : attn_kstr(m.D)), (cuuint32_t)kAttnChunk, 1, 1};
+    const CUresult r = encode(kv ? &b.tm_v : &b.tm_k, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kv ? b.vcache : b.kcache,
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t attn_configure(const ModelDims& m, size_t smem) {
   DecoderBufs b{};
   return attn_any(m.D, m.Hq / m.Hkv, true, smem, b, m, 1, 0, nullptr);
@@ -987,6 +1165,11 @@ cudaError_t launch_attention(const DecoderBufs& b, const ModelDims& m, int N, in
   return launch_pdl(k_quant_slices<0>, dim3(N, (QD + kQuantSlice - 1) / kQuantSlice), dim3(kQuantSlice / 4), 0, st,
                     (const SpecCtl*)b.ctl, (const float*)b.qkv, QD, QD, (const float2*)b.qpart, m.Hq, 0.0f, b.act, N,
                     b.a_s);
+}
+
+cudaError_t launch_tree_attention(const DecoderBufs& b, const ModelDims& m, int N, int layer, cudaStream_t st) {
+  const int G = m.Hq / m.Hkv;
+  return attn_any(m.D, G, false, attn_smem_bytes(m.D, N * G), b, m, N, layer, st);
 }
 
 cudaError_t launch_swiglu_quant(const DecoderBufs& b, const ModelDims& m, int N, int gu_S, cudaStream_t st) {

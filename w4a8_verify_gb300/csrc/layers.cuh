@@ -6,6 +6,8 @@ namespace w4a8 {
 
 size_t attn_smem_bytes(int D, int Nq);
 cudaError_t attn_configure(const ModelDims& m, size_t smem);
+// encodes b.tm_k and b.tm_v (the caches must be allocated)
+cudaError_t attn_tensor_maps(DecoderBufs& b, const ModelDims& m);
 
 cudaError_t launch_embed(const DecoderBufs& b, const ModelDims& m, int N, const uint32_t* ew, const uint16_t* es,
                          cudaStream_t st);
@@ -16,6 +18,8 @@ cudaError_t launch_rmsnorm_quant(const DecoderBufs& b, const ModelDims& m, int N
 // the QKV projection's output comes from its qkv_S EPI_PARTIAL slices in b.mm_part
 cudaError_t launch_rope_kv(const DecoderBufs& b, const ModelDims& m, int N, int layer, int qkv_S, cudaStream_t st);
 cudaError_t launch_attention(const DecoderBufs& b, const ModelDims& m, int N, int layer, cudaStream_t st);
+// the tree attention pass alone: queries b.qrot -> attention output in b.qkv ([N][Hq*D])
+cudaError_t launch_tree_attention(const DecoderBufs& b, const ModelDims& m, int N, int layer, cudaStream_t st);
 // gate|up from the gu_S EPI_PARTIAL slices in b.mm_part
 cudaError_t launch_swiglu_quant(const DecoderBufs& b, const ModelDims& m, int N, int gu_S, cudaStream_t st);
 // logits from the lm_S EPI_PARTIAL slices of the head projection in b.mm_part (folded here and

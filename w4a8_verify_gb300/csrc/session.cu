@@ -356,6 +356,7 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
   e = e == cudaSuccess ? cudaEventCreateWithFlags(&s->ev[1], cudaEventDisableTiming) : e;
   e = e == cudaSuccess ? cudaStreamCreateWithFlags(&s->cap, cudaStreamNonBlocking) : e;
   e = e == cudaSuccess ? attn_configure(d, attn_smem_bytes(d.D, kMaxWidth * (d.Hq / d.Hkv))) : e;
+  e = e == cudaSuccess ? attn_tensor_maps(b, d) : e;
   e = e == cudaSuccess ? mm_configure() : e;
   e = e == cudaSuccess ? draft_configure(desc->ctx_cap) : e;
   if (e != cudaSuccess) {
@@ -848,6 +849,27 @@ W4A8_API w4a8_status w4a8_session_get_context(w4a8_session* s, int32_t* out, int
   *n = (int)c.ctx_len;
   const int k = std::min(cap, (int)c.ctx_len);
   if (k > 0) return sync_read(s, out, s->b.ctx, (size_t)k * 4);
+  return W4A8_OK;
+}
+
+W4A8_API w4a8_status w4a8_session_attention(w4a8_session* s, int layer, int n, const float* q, float* out,
+                                            void* stream) {
+  if (!s || !q || !out || layer < 0 || layer >= s->m->d.n_layers || n < 1 || n > kMaxWidth) return W4A8_ERR_ARG;
+  const ModelDims& d = s->m->d;
+  cudaStream_t cs = as_stream(stream);
+  // the kernel reads slots [0, committed_len + n): check the control state first
+  W4A8_CUDA_TRY(cudaStreamSynchronize(cs));
+  SpecCtl ctl;
+  TreeState tree;
+  W4A8_CUDA_TRY(cudaMemcpy(&ctl, s->b.ctl, sizeof(ctl), cudaMemcpyDeviceToHost));
+  W4A8_CUDA_TRY(cudaMemcpy(&tree, s->b.tree, sizeof(tree), cudaMemcpyDeviceToHost));
+  if ((ctl.flags & FLAG_STOP_MASK) != 0u) return W4A8_ERR_DEVICE_FLAG;
+  if ((long long)ctl.committed_len + n > s->b.kv_cap) return W4A8_ERR_CAPACITY;
+  if (n > tree.n_valid) return W4A8_ERR_ARG;
+  const size_t qn = (size_t)n * d.Hq * d.D;
+  W4A8_CUDA_TRY(cudaMemcpyAsync(s->b.qrot, q, qn * 4, cudaMemcpyDeviceToDevice, cs));
+  W4A8_CUDA_TRY(launch_tree_attention(s->b, d, n, layer, cs));
+  W4A8_CUDA_TRY(cudaMemcpyAsync(out, s->b.qkv, qn * 4, cudaMemcpyDeviceToDevice, cs));
   return W4A8_OK;
 }
 
