@@ -321,6 +321,7 @@ __global__ void __maxnreg__(168)
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_path[kMaxWidth][kMaxWidth];
   __shared__ int s_dep[kMaxWidth], s_par[kMaxWidth];
+  __shared__ int s_row[kMaxWidth];  // tree row at depth e shared by every node that deep, or -1
   __shared__ float s_cs[kMaxWidth * 8];  // per-query rescale c of the running values (this chunk)
   __shared__ float s_M[kMaxWidth * 8], s_L[kMaxWidth * 8];  // running max and sum per query
   __shared__ uint64_t full[NE], empty[NE];
@@ -425,6 +426,18 @@ __global__ void __maxnreg__(168)
       }
     return;
   }
+  // slot L + e of every node that deep holds the same row (a chain, or a shared prefix)?
+  if (threadIdx.x <= maxd) {
+    const int e = threadIdx.x;
+    int r = -1;
+    bool same = true;
+    for (int i = 0; i < N; ++i)
+      if (s_dep[i] >= e) {
+        if (r < 0) r = s_path[i][e];
+        else same = same && s_path[i][e] == r;
+      }
+    s_row[e] = same ? r : -1;
+  }
   // queries of the KV head (the G heads of kh are consecutive in qrot) and the tree rows
   // (slots L .. L+N-1, read by the chunks that reach past L), both written by the kernel
   // just before this one; every load is issued before the first split.
@@ -494,6 +507,12 @@ __global__ void __maxnreg__(168)
     for (int nn = 0; nn < NTW; ++nn)
 #pragma unroll
       for (int e = 0; e < 4; ++e) Or[m][nn][e] = 0.0f;
+  // Every tree slot holds one row for all the nodes that see it (a chain of several nodes,
+  // say): then chunks reaching past the cache also take one B for all queries, the tree slots
+  // reading that row (a key a query does not see is masked, a value it does not see has
+  // weight zero).  Either way a row sees the same operations on the same values.
+  bool merged = N > 1;
+  for (int e = 0; e <= maxd; ++e) merged = merged && s_row[e] >= 0;
   bool ok = true;
   int n = 0;  // ring entries consumed
   for (int c = c_begin; c < c_end; ++c, n += 2) {
@@ -543,6 +562,41 @@ __global__ void __maxnreg__(168)
               const float* kr = Ks + (size_t)(8 * (nt0 + i) + lg) * KSTR + st * 16 + 2 * lt;
               const float2 k0 = *reinterpret_cast<const float2*>(kr);
               const float2 k1 = *reinterpret_cast<const float2*>(kr + 8);
+              uint32_t bh0, bl0, bh1, bl1;
+              split_h2(k0.x, k0.y, bh0, bl0);
+              split_h2(k1.x, k1.y, bh1, bl1);
+              mma_split3(acc[i], ah, al, bh0, bh1, bl0, bl1);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < NTPW; ++i) store(acc[i], mw, nt0 + i, -1);
+        }
+      } else if (merged) {
+        // chunk reaching past the cache with shared tree slots: the same partition, each lane's
+        // key row from the cache, the shared tree row, or zero (past every node)
+        const int mw = warp / WPM, nt0 = (warp % WPM) * NTPW;
+        if (mw < nmt) {
+          float acc[NTPW][4];
+          const float* krow[NTPW];
+#pragma unroll
+          for (int i = 0; i < NTPW; ++i) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[i][e] = 0.0f;
+            const int j = 8 * (nt0 + i) + lg;
+            krow[i] = j < jc ? Ks + (size_t)j * KSTR
+                             : (P0 + j - L <= maxd ? Kt + (size_t)s_row[P0 + j - L] * D : nullptr);
+          }
+#pragma unroll
+          for (int st = 0; st < KS; ++st) {
+            const uint4* af = reinterpret_cast<const uint4*>(Qf + ((size_t)(mw * KS + st) * 32 + lane) * 32);
+            const uint4 ah = af[0], al = af[1];
+#pragma unroll
+            for (int i = 0; i < NTPW; ++i) {
+              float2 k0 = make_float2(0.0f, 0.0f), k1 = make_float2(0.0f, 0.0f);
+              if (krow[i] != nullptr) {
+                k0 = *reinterpret_cast<const float2*>(krow[i] + st * 16 + 2 * lt);
+                k1 = *reinterpret_cast<const float2*>(krow[i] + st * 16 + 2 * lt + 8);
+              }
               uint32_t bh0, bl0, bh1, bl1;
               split_h2(k0.x, k0.y, bh0, bl0);
               split_h2(k1.x, k1.y, bh1, bl1);
@@ -737,7 +791,8 @@ __global__ void __maxnreg__(168)
         split_h2(x2, x3, bh1, bl1);
       };
       // steps past the last slot that any node sees add nothing (their weights are zero); the
-      // leading steps whose 16 slots are all cached take one B for all queries
+      // leading steps whose 16 slots are all cached (every step, when the tree slots are
+      // shared) take one B for all queries
       const int nst = min(CH - 1, L + maxd - P0) / 16 + 1;
       const int ncs = min(nst, max(jc, 0) / 16);
 #pragma unroll
@@ -761,7 +816,29 @@ __global__ void __maxnreg__(168)
       }
       for (int st = ncs; st < nst; ++st) {
         const int js = st * 16 + 2 * lt;
-        {
+        if (merged) {
+          // shared tree slots: one B for all queries, rows from the cache, the shared tree row or
+          // zero (past every node)
+          auto vshared = [&](int jj) -> const float* {
+            if (jj < jc) return Vs + (size_t)jj * VSTR;
+            return P0 + jj - L <= maxd ? Vt + (size_t)s_row[P0 + jj - L] * D : nullptr;
+          };
+          const float* r0 = vshared(js);
+          const float* r1 = vshared(js + 1);
+          const float* r2 = vshared(js + 8);
+          const float* r3 = vshared(js + 9);
+          uint32_t bh0[NTW], bl0[NTW], bh1[NTW], bl1[NTW];
+#pragma unroll
+          for (int nn = 0; nn < NTW; ++nn) vfrag(r0, r1, r2, r3, nn, bh0[nn], bl0[nn], bh1[nn], bl1[nn]);
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            if (m >= nmt) break;
+            const uint4* af = reinterpret_cast<const uint4*>(EF + ((size_t)(m * VS + st) * 32 + lane) * 8);
+            const uint4 ah = af[0], al = af[1];
+#pragma unroll
+            for (int nn = 0; nn < NTW; ++nn) mma_split3(Or[m][nn], ah, al, bh0[nn], bh1[nn], bl0[nn], bl1[nn]);
+          }
+        } else {
           // per node: its own rows for the slots of this step (cache below jc, ancestors from
           // L on, zero past the node); four nodes at a time
           auto vrow = [&](int node, int kk) -> const float* {
