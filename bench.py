@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama3-8b-ctx4096", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--new-tokens", type=int, default=MAX_NEW,
+                    help="tokens generated per step (the workload's figure is %d)" % MAX_NEW)
     ap.add_argument("--matmul", type=int, nargs=3, metavar=("K", "N", "M"),
                     help="time one W4A8 matmul shape through the C ABI instead of the decoding step")
     return ap.parse_args()
@@ -439,7 +441,9 @@ def run_reference(args, rank, world):
 
 
 def main():
+    global MAX_NEW
     args = parse()
+    MAX_NEW = args.new_tokens
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
     if args.impl == "reference":
