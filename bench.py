@@ -211,8 +211,9 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     t_build = time.time() - t0
     prompt = synth.motif_prompt(seed, plen, nmot, mlen, psub, shape.vocab)
-    kv_cap = plen + MAX_NEW + 32
-    ctx_cap = plen + MAX_NEW + 64
+    room = max(MAX_NEW, 64)  # the window-size probe below generates 64 tokens
+    kv_cap = plen + room + 32
+    ctx_cap = plen + room + 64
     sess = W.Session(model, kv_cap, ctx_cap, max_window=16)
     prompt_dev = torch.from_numpy(prompt).to(dev)
     stream = torch.cuda.current_stream()
