@@ -10,7 +10,7 @@
   ("GPU-Resident Speculative Decoding ...", Design > Small-Batch Verification
   Kernels says per block of 32; the per-token absmax reading is the default).
 
-Readings where the pages are silent (listed in the design doc as well):
+Readings where the pages are silent:
 * weight scale s = fp16(fp32(absmax) / 7), code q = clamp(rint(w / s), -8, 7)
   with rint = round half to even, taken in fp32; absmax = 0 (or s rounding to
   0) gives s = 0 and q = 0.

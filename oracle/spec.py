@@ -18,7 +18,7 @@ position with the current suffix at orders up to 8, selection of the best
 positions, a weighted trie of their continuations, emission of the most
 probable prefix-closed node set.
 
-Readings where the pages leave a step open (also in the design doc):
+Readings where the pages leave a step open:
 * matched positions p in [0, n-2]; l(p) = largest l <= 8 with
   c[p-l+1..p] == c[n-l..n-1]; candidates are the 16 best by (l desc, p desc)
   among l >= 1; a candidate continues with c[p+1 .. min(p+8, n-1)] with weight
