@@ -270,22 +270,24 @@ __device__ __forceinline__ void mma_split3(float (&d)[4], uint4 ahi, uint4 alo, 
 
 // Attention pass, grid (split sp, KV head kh).  Chunks of kAttnChunk logical positions are
 // dealt to the splits in contiguous ranges of R (R and the split count depend on the cache
-// capacity and the head count only).  The CTA streams each chunk's cached K and V rows
-// (contiguous) through a ring of 2 * kAttnStages cp.async.bulk entries and keeps, for every
-// query of the KV head (node i, head g; q = i*G + g), a running (M, L, O) over its chunks in
-// ascending order:
+// capacity and the head count only).  A copy warp brings each chunk's cached K and V rows
+// into a ring of 2 * kAttnStages entries with one TMA box each (rows at padded strides); the
+// compute warps keep, for every query of the KV head (node i, head g; q = i*G + g), a running
+// (M, L, O) over its chunks in ascending order:
 //   scores: s = q . k on the tensor cores (mma m16n8k16, f32 accumulation) from the f16 splits
 //           q = qh + ql, k = kh + kl: per 16-dimension step qh.kh + qh.kl + ql.kh, steps in order
 //           (the row of a score depends on its own query and key only);
 //   per chunk: m = max(M, max over visible slots), c = exp(M - m), e_j = exp(s_j - m),
 //           L = L * c + (butterfly sum of e over the 64 slots, lane l holding slots 2l, 2l+1);
-//   values: the chunk sum P[d] = sum_j e_j v_j[d] on the tensor cores from the f16 splits
-//           e = eh + el, v = vh + vl: per 16-slot step eh.vh + eh.vl + el.vh, steps in order,
-//           then O[d] = fmaf(O[d], c, P[d]); M = m.
+//   values: O = O * c, then O += e . v on the tensor cores from the f16 splits of 2^15 e and
+//           of v (per 16-slot step eh.vh + eh.vl + el.vh, steps in order; the exact factor
+//           2^15 is removed when the partial is stored); M = m.
 // Slots below the committed length L read the cache; slots at L + e read the node's
-// ancestor at depth e (tree rows); a 16-slot group reaching past the cache is multiplied
-// with each node's own rows (zero rows past the node), keeping that node's rows of the
-// result, so every row sees the same operations as in a step where those slots are cached.
+// ancestor at depth e (tree rows).  A 16-key or 16-slot group reaching past the cache is
+// multiplied with each node's own rows (zero rows past the node), keeping that node's rows
+// of the result; when every tree slot holds one row for all the nodes that see it, that row
+// serves every query (a key a query does not see is masked, a value has weight zero).  Either
+// way every row sees the same operations as in a step where those slots are cached.
 // The last CTA of a KV head to finish (ticket) merges the splits of every query in ascending
 // order (M = max M_s, L = sum exp(M_s - M) L_s, O = sum exp(M_s - M) O_s), writes O / L and
 // the per-(node, head) maximum |O / L| that the quantiser of the O projection reads (MERGE;
