@@ -299,6 +299,25 @@ def run_ours(args, rank, world):
     achieved = bytes1 / us1 / 1e3
     trf = mm_traffic(os.path.join(ROOT, "w4a8_verify_gb300", "csrc", "matmul.cu"))
 
+    # decode modes of the pages' comparison on the same prompt and token count (not part of
+    # `value`): greedy with a host read-back after every token, the GPU loop at width 1 in
+    # windows of 8, and the speculation loop with the controller (= value)
+    modes = {}
+    for name, kw in (("greedy_host_sync_per_token", dict(window=1, fixed_width=1, in_flight=1)),
+                     ("gpu_loop_width1_window8", dict(window=8, fixed_width=1, in_flight=2))):
+        try:
+            sess.prefill(prompt_dev, MAX_NEW)
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            ev0.record(stream)
+            toks_m, _ = sess.generate(MAX_NEW, **kw)
+            ev1.record(stream)
+            ev1.synchronize()
+            modes[name] = round(len(toks_m) / (ev0.elapsed_time(ev1) / 1e3), 2)
+        except Exception as exc:  # reported, never fatal to the line
+            modes[name] = "failed: %s" % exc
+    modes["spec_controller"] = round(value, 2)
+
     launches = sum(int(r.kernels) for r in reps)  # kernel nodes of the window graphs run while timed
     mean_rep = reps[-1]
     steps_total = sum(r.n_steps for r in reps)
@@ -343,6 +362,7 @@ def run_ours(args, rank, world):
                          for N, v in mm.items()},
         },
         "verify_step_us": {str(w): round(t, 1) for w, t in zip(WIDTHS, t_us)},
+        "decode_modes_tokens_per_s": modes,
         "verify_ratio_8_over_1": round(t_us[2] / t_us[0], 3),
         "tau_tokens_per_step": round(MAX_NEW * args.steps / max(1, steps_total), 3),
         "width_steps": wsteps,
