@@ -20,8 +20,16 @@ KV head h // (Hq / Hkv); rope is rotate-half with theta_i = base^(-2i/d).
 
 Arithmetic is fp64; K and V are stored in fp32 (the pages' KV precision); the
 int8 code decisions are taken in fp32 (``oracle.quant``).  Every per-token
-quantity is computed row by row, so a token's result does not depend on how
-many tokens share the call.
+quantity is computed row by row (each row quantised on its own, each product a
+matrix-vector product), so a token's result does not depend on how many tokens
+share the call.
+
+Quantisation points ("stages") of one token, in evaluation order: for every layer
+l, ``l{l}.n1`` (RMSNorm output before Q/K/V), ``l{l}.att`` (attention output before
+O), ``l{l}.n2`` (RMSNorm output before gate/up), ``l{l}.sw`` (SwiGLU output before
+down); then ``lm`` (final RMSNorm output before the LM head).  With ``record`` set,
+the model keeps, per (cache slot, stage), the int8 codes and the distance of every
+code's decision to its rounding boundary (``decision_margins``).
 """
 from __future__ import annotations
 
@@ -33,6 +41,11 @@ from . import quant as Q
 
 import synth
 
+# dequantised weights are cached while the model's total stays below this; larger
+# models dequantise each product in row blocks (same values, bounded memory)
+DEQ_CACHE_BYTES = 1 << 30
+DEQ_BLOCK_ELEMS = 1 << 25
+
 
 @dataclasses.dataclass
 class Weights:
@@ -40,6 +53,8 @@ class Weights:
     layers: list          # per layer: dict kind -> (codes int8 [rows][cols], scales fp16 [rows][cols/32])
     embed: tuple
     lm_head: tuple
+    # dequantised fp64 weights shared by the Models built on these weights (when cached)
+    deq_cache: dict = dataclasses.field(default_factory=dict, repr=False)
 
 
 def build_weights(shape, seed: int) -> Weights:
@@ -60,6 +75,23 @@ def build_weights(shape, seed: int) -> Weights:
     else:
         lm = Q.quantize_weights_g32(synth.dense_weight(shape, seed, synth.STREAM_LM_HEAD, V, H, V, H))
     return Weights(shape, layers, emb, lm)
+
+
+def stage_names(n_layers: int) -> list:
+    """The quantisation points of one token in evaluation order."""
+    out = []
+    for l in range(n_layers):
+        out += ["l%d.n1" % l, "l%d.att" % l, "l%d.n2" % l, "l%d.sw" % l]
+    return out + ["lm"]
+
+
+def stage_width(shape, stage: str) -> int:
+    """Inputs quantised at a stage."""
+    if stage.endswith(".att"):
+        return shape.n_heads * shape.head_dim
+    if stage.endswith(".sw"):
+        return shape.ffn
+    return shape.hidden
 
 
 def rmsnorm(x: np.ndarray, eps: float) -> np.ndarray:
@@ -102,47 +134,83 @@ def quant_row(x: np.ndarray):
     return q[0], s[0]
 
 
-def decision_margin(x: np.ndarray) -> float:
-    """Distance, in code units, from the closest int8 decision of quant_row(x) to a rounding
-    boundary (k + 1/2).  A second evaluation whose inputs differ in the last bits can only
-    take a different code where this is small.  Diagnostic only."""
+def decision_margins(x: np.ndarray) -> np.ndarray:
+    """Per input of quant_row(x): the distance, in code units, of its fp32 quotient
+    r = |x_k| / s from the nearest rounding boundary k + 1/2 of the round-to-nearest
+    decision (0.5 = the middle between two boundaries).  Inputs whose quotient reaches
+    the clamp at 127 have no rounding boundary above it and take the distance to the one
+    below.  A second evaluation of the same definition whose inputs differ from these by
+    less than the margin (in code units) takes the same code.  An all-zero row has no
+    decision (infinite margins)."""
     x32 = np.asarray(x, dtype=np.float32)
     _, s = Q.quantize_act_per_token(x32[None, :])
     if s[0] == 0:
-        return np.inf
+        return np.full(x32.shape, np.inf)
     r = np.abs(x32.astype(np.float64)) / np.float64(s[0])
-    r = r[r < 127.0]
-    if r.size == 0:
-        return np.inf
-    return float(np.min(np.abs(r - np.floor(r) - 0.5)))
+    r = np.minimum(r, 127.0)
+    return np.abs(r - np.floor(r) - 0.5)
+
+
+def decision_margin(x: np.ndarray) -> float:
+    """Smallest of ``decision_margins(x)``."""
+    return float(np.min(decision_margins(x)))
 
 
 class Model:
     """A quantised decoder with an fp32 KV cache of ``kv_cap`` slots per layer."""
 
-    def __init__(self, weights: Weights, kv_cap: int):
+    def __init__(self, weights: Weights, kv_cap: int, record: bool = False, cache_bytes=None):
         self.w = weights
         self.shape = sh = weights.shape
         self.kv_cap = kv_cap
         self.K = [np.zeros((sh.n_kv_heads, kv_cap, sh.head_dim), np.float32) for _ in range(sh.n_layers)]
         self.V = [np.zeros((sh.n_kv_heads, kv_cap, sh.head_dim), np.float32) for _ in range(sh.n_layers)]
-        self._dq = {}
-        # diagnostic: smallest int8 decision margin of the token held in each cache slot
-        self.margin = np.full(kv_cap, np.inf)
-        self._m = np.inf
+        self._dq = weights.deq_cache
+        total = sum(q.size for d in weights.layers for q, _ in d.values()) + weights.lm_head[0].size
+        self._cache_deq = total * 8 <= (DEQ_CACHE_BYTES if cache_bytes is None else cache_bytes)
+        # (slot, stage) -> (codes int8 [K], margins fp64 [K]) of the last evaluation at that slot
+        self.record = {} if record else None
 
     # -- weights -----------------------------------------------------------
-    def _deq(self, key, qs):
-        if key not in self._dq:
-            self._dq[key] = Q.dequantize_weights(qs[0], qs[1])
-        return self._dq[key]
+    def _deq(self, key, qs, r0=None, r1=None):
+        if r0 is None:
+            if self._cache_deq:
+                if key not in self._dq:
+                    self._dq[key] = Q.dequantize_weights(qs[0], qs[1])
+                return self._dq[key]
+            return Q.dequantize_weights(qs[0], qs[1])
+        if self._cache_deq:
+            return self._deq(key, qs)[r0:r1]
+        return Q.dequantize_weights(qs[0][r0:r1], qs[1][r0:r1])
+
+    def products(self, key, qs, A: np.ndarray) -> np.ndarray:
+        """W4A8 products of already quantised (dequantised, exact in fp64) activation rows
+        A [n][K]: every row is its own matrix-vector product with the fp64 weights."""
+        rows, cols = qs[0].shape
+        n = A.shape[0]
+        out = np.zeros((n, rows))
+        blk = max(1, DEQ_BLOCK_ELEMS // cols)
+        for r0 in range(0, rows, blk):
+            r1 = min(rows, r0 + blk)
+            Wb = self._deq(key, qs, r0, r1)
+            for i in range(n):
+                out[i, r0:r1] = Wb @ A[i]
+        return out
+
+    def quantize(self, X: np.ndarray, stage=None, slots=None) -> np.ndarray:
+        """Per-row int8 quantisation (decisions in fp32); returns the dequantised rows
+        (codes times scale, exact in fp64).  Records codes and margins when enabled."""
+        out = np.zeros(X.shape)
+        for i in range(X.shape[0]):
+            q, s = quant_row(X[i])
+            out[i] = q.astype(np.float64) * np.float64(s)
+            if self.record is not None and stage is not None:
+                self.record[(int(slots[i]), stage)] = (q.copy(), decision_margins(X[i]))
+        return out
 
     def linear(self, key, qs, x_row: np.ndarray) -> np.ndarray:
         """W4A8 product of one activation row: quantise, then the exact-operand fp64 product."""
-        self._m = min(self._m, decision_margin(x_row))
-        q, s = quant_row(x_row)
-        a = q.astype(np.float64) * np.float64(s)
-        return self._deq(key, qs) @ a
+        return self.products(key, qs, self.quantize(np.asarray(x_row, dtype=np.float64)[None, :]))[0]
 
     def embed(self, tok: int) -> np.ndarray:
         q, s = self.w.embed
@@ -150,50 +218,50 @@ class Model:
         return q[tok].astype(np.float64) * np.repeat(s[tok].astype(np.float64), Q.GROUP)[:H]
 
     # -- forward -------------------------------------------------------------
-    def forward(self, toks, pos, slots, visible, trace=None) -> np.ndarray:
+    def forward(self, toks, pos, slots, visible, trace=None, head: bool = True):
         """Evaluate tokens ``toks`` at logical positions ``pos``; write their K/V to cache
         ``slots``; token i attends to the cache slots ``visible[i]`` (given in logical
-        order, all written before attention).  Returns fp64 logits [n][vocab].
-        ``trace`` (a dict) collects per-layer intermediates for the tests."""
+        order, all written before attention).  Returns fp64 logits [n][vocab] (None when
+        ``head`` is False).  ``trace`` (a dict) collects per-layer intermediates for the
+        tests."""
         sh = self.shape
         n = len(toks)
         H, Hq, Hkv, d = sh.hidden, sh.n_heads, sh.n_kv_heads, sh.head_dim
+        eps = sh.rms_eps
         x = np.stack([self.embed(int(t)) for t in toks])
-        tok_m = np.full(n, np.inf)
         for l, Wl in enumerate(self.w.layers):
+            A = self.quantize(np.stack([rmsnorm(x[i], eps) for i in range(n)]), "l%d.n1" % l, slots)
+            qv = self.products((l, synth.T_WQ), Wl[synth.T_WQ], A).reshape(n, Hq, d)
+            kv = self.products((l, synth.T_WK), Wl[synth.T_WK], A).reshape(n, Hkv, d)
+            vv = self.products((l, synth.T_WV), Wl[synth.T_WV], A).reshape(n, Hkv, d)
             qh = np.zeros((n, Hq, d))
             for i in range(n):
-                self._m = tok_m[i]
-                n1 = rmsnorm(x[i], sh.rms_eps)
-                qv = self.linear((l, synth.T_WQ), Wl[synth.T_WQ], n1).reshape(Hq, d)
-                kv = self.linear((l, synth.T_WK), Wl[synth.T_WK], n1).reshape(Hkv, d)
-                vv = self.linear((l, synth.T_WV), Wl[synth.T_WV], n1).reshape(Hkv, d)
-                qh[i] = rope(qv, int(pos[i]), sh.rope_base)
-                self.K[l][:, int(slots[i])] = rope(kv, int(pos[i]), sh.rope_base).astype(np.float32)
-                self.V[l][:, int(slots[i])] = vv.astype(np.float32)
-                tok_m[i] = self._m
+                qh[i] = rope(qv[i], int(pos[i]), sh.rope_base)
+                self.K[l][:, int(slots[i])] = rope(kv[i], int(pos[i]), sh.rope_base).astype(np.float32)
+                self.V[l][:, int(slots[i])] = vv[i].astype(np.float32)
+            att = np.zeros((n, Hq, d))
             for i in range(n):
-                self._m = tok_m[i]
                 vis = np.asarray(visible[i], dtype=np.int64)
-                att = np.zeros((Hq, d))
                 for h in range(Hq):
                     kh = kv_head_of(h, Hq, Hkv)
-                    att[h] = attend(qh[i, h], self.K[l][kh, vis], self.V[l][kh, vis])
-                hrow = x[i] + self.linear((l, synth.T_WO), Wl[synth.T_WO], att.reshape(-1))
-                mlp = self.mlp(l, Wl, rmsnorm(hrow, sh.rms_eps))
-                if trace is not None:
-                    trace.setdefault("att", []).append(att.copy())
-                    trace.setdefault("h", []).append(hrow.copy())
-                    trace.setdefault("mlp", []).append(mlp.copy())
-                x[i] = hrow + mlp
-                tok_m[i] = self._m
-        logits = np.zeros((n, sh.vocab))
-        for i in range(n):
-            self._m = tok_m[i]
-            logits[i] = self.linear("lm", self.w.lm_head, rmsnorm(x[i], sh.rms_eps))
-            tok_m[i] = self._m
-            self.margin[int(slots[i])] = tok_m[i]
-        return logits
+                    att[i, h] = attend(qh[i, h], self.K[l][kh, vis], self.V[l][kh, vis])
+            A = self.quantize(att.reshape(n, Hq * d), "l%d.att" % l, slots)
+            hrow = x + self.products((l, synth.T_WO), Wl[synth.T_WO], A)
+            A = self.quantize(np.stack([rmsnorm(hrow[i], eps) for i in range(n)]), "l%d.n2" % l, slots)
+            g = self.products((l, synth.T_WG), Wl[synth.T_WG], A)
+            u = self.products((l, synth.T_WU), Wl[synth.T_WU], A)
+            A = self.quantize(silu(g) * u, "l%d.sw" % l, slots)
+            mlp = self.products((l, synth.T_WD), Wl[synth.T_WD], A)
+            if trace is not None:
+                for i in range(n):
+                    trace.setdefault("att", []).append(att[i].copy())
+                    trace.setdefault("h", []).append(hrow[i].copy())
+                    trace.setdefault("mlp", []).append(mlp[i].copy())
+            x = hrow + mlp
+        if not head:
+            return None
+        A = self.quantize(np.stack([rmsnorm(x[i], eps) for i in range(n)]), "lm", slots)
+        return self.products("lm", self.w.lm_head, A)
 
     def mlp(self, l, Wl, n2) -> np.ndarray:
         """SwiGLU block on a normalised row: quant(silu(gate) * up) -> down projection."""
@@ -202,10 +270,11 @@ class Model:
         return self.linear((l, synth.T_WD), Wl[synth.T_WD], silu(g) * u)
 
     # -- protocols -------------------------------------------------------------
-    def prefill(self, toks) -> np.ndarray:
+    def prefill(self, toks, head: bool = True):
         """Causal pass over ``toks`` at positions/slots 0..n-1."""
         n = len(toks)
-        return self.forward(toks, list(range(n)), list(range(n)), [list(range(i + 1)) for i in range(n)])
+        return self.forward(toks, list(range(n)), list(range(n)), [list(range(i + 1)) for i in range(n)],
+                            head=head)
 
     def step(self, tok: int, L: int) -> np.ndarray:
         """One plain decoding step: token at position/slot L attending to slots 0..L."""
@@ -224,7 +293,7 @@ def greedy_decode(weights: Weights, prompt, max_new: int, eos: int = -1, kv_cap:
     n = len(prompt)
     m = Model(weights, kv_cap or (n + max_new + 1))
     if n > 1:
-        m.prefill(prompt[:-1])
+        m.prefill(prompt[:-1], head=False)
     L, tok = n - 1, prompt[-1]
     out, logits = [], []
     while len(out) < max_new:
@@ -236,3 +305,20 @@ def greedy_decode(weights: Weights, prompt, max_new: int, eos: int = -1, kv_cap:
         if tok == eos:
             break
     return out, logits
+
+
+def teacher_forced_logits(weights: Weights, prompt, forced, kv_cap: int | None = None):
+    """Logits of plain decoding steps whose inputs are the given tokens: prefill
+    prompt[:-1], then steps on prompt[-1], forced[0], forced[1], ...  Returns the
+    fp64 logits of each step (len(forced) + 1 rows)."""
+    prompt = [int(t) for t in prompt]
+    n = len(prompt)
+    m = Model(weights, kv_cap or (n + len(forced) + 2))
+    if n > 1:
+        m.prefill(prompt[:-1], head=False)
+    out = []
+    L = n - 1
+    for tok in [prompt[-1]] + [int(t) for t in forced]:
+        out.append(m.step(tok, L))
+        L += 1
+    return out

@@ -191,7 +191,7 @@ def spec_decode(weights, prompt, max_new: int, widths, eos: int = -1, kv_cap: in
     nmax = 32
     m = Model(weights, kv_cap or (n + max_new + nmax + 1))
     if n > 1:
-        m.prefill(prompt[:-1])
+        m.prefill(prompt[:-1], head=False)
     L_c = n - 1
     ctx = list(prompt)
     out, stats = [], []

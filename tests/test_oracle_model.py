@@ -154,3 +154,44 @@ def test_tree_verify_equals_sequential_root_paths(tiny_weights, seed):
         path = OS.ancestors_or_self(parent, i)
         ref = OM.Model(tiny_weights, L_c + 20).prefill(ctx + [int(tok[j]) for j in path])[-1]
         assert np.array_equal(lg[i], ref), i
+
+
+def test_decision_margins_closed_form():
+    # amax 127 -> scale exactly 1.0, so the quotient of every input is the input itself
+    x = np.array([127.0, 10.3, -5.51, 2.5, 0.0, -126.2], dtype=np.float32)
+    m = OM.decision_margins(x)
+    f = x.astype(np.float64)
+    assert m[0] == 0.5                                   # at the clamp: distance to 126.5
+    assert np.isclose(m[1], abs(10.3 - 10.5), atol=1e-6) and abs(m[1] - 0.2) < 1e-6
+    assert m[2] == abs(abs(f[2]) - 5.5) and 0.0099 < m[2] < 0.0101   # sign does not matter
+    assert m[3] == 0.0                                   # exactly on a rounding boundary
+    assert m[4] == 0.5                                   # zero: midway between -1/2 and 1/2
+    assert np.isclose(m[5], 0.3, atol=1e-5)
+    assert OM.decision_margin(x) == 0.0
+    assert OM.decision_margin(x[[0, 1, 2]]) == m[2]
+    # scale 2: quotient = x / 2
+    y = np.array([254.0, 5.0, 7.2], dtype=np.float32)
+    my = OM.decision_margins(y)
+    assert my[1] == 0.0 and np.isclose(my[2], 0.1, atol=1e-6)
+    assert np.all(np.isinf(OM.decision_margins(np.zeros(8, np.float32))))
+
+
+def test_decision_margin_predicts_code_changes():
+    # a perturbation smaller than an input's margin (in code units) keeps its code; one
+    # larger than the margin, towards the boundary, changes it
+    rng = np.random.default_rng(11)
+    x = rng.normal(size=256).astype(np.float32)
+    q0, s = OM.quant_row(x)
+    m = OM.decision_margins(x)
+    k = int(np.argmin(m[np.abs(x) < np.abs(x).max()]))
+    k = int(np.flatnonzero(np.abs(x) < np.abs(x).max())[k])
+    r = abs(float(x[k])) / float(s)
+    towards = np.sign(r - np.floor(r) - 0.5) * -np.sign(x[k])   # direction of the boundary
+    y = x.astype(np.float64).copy()
+    y[k] += towards * (m[k] + 1e-4) * float(s)
+    q1, s1 = OM.quant_row(y)
+    assert s1 == s and abs(int(q1[k]) - int(q0[k])) == 1
+    z = x.astype(np.float64).copy()
+    z[k] += towards * 0.5 * m[k] * float(s)
+    q2, _ = OM.quant_row(z)
+    assert np.array_equal(q2, q0)

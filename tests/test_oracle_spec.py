@@ -267,3 +267,64 @@ def test_tree_attention_uses_the_grouped_kv_head():
     out = OS.tree_attention(qs, K, V, 5, [-1, 0, 1, 1, 0, 4])
     assert np.all(out[:, 2:] == 0.0)
     assert np.all(np.abs(out[:, :2]).sum(axis=-1) > 0)
+
+
+# ---------------------------------------------------------------- drafter scoring pins
+# Draft-Free Drafting From Web Context: candidates are weighted by a fixed function of
+# their match length (read: w = l), at most 16 candidates are kept (most recent first
+# among equal lengths), and trie nodes are taken best-first by (score desc, depth asc,
+# insertion asc).  Each context below is built so that one plausible misreading picks a
+# different first node; the match lengths it relies on are asserted first.
+
+def test_draft_weight_is_match_length_not_count():
+    X, Y, Z, A, B = 101, 102, 103, 104, 105
+    ctx = [X, Y, Z, A, 7, Z, B, 8, Z, B, 9, X, Y, Z]
+    ell = OS.match_lengths(ctx)
+    assert ell[2] == 3 and ell[5] == 1 and ell[8] == 1
+    assert sorted(int(v) for v in ell if v > 0) == [1, 1, 3]
+    tok, parent, n_valid, best = OS.draft(ctx, 2)
+    # w = l: A scores 3 against B's 1 + 1; a count (w = 1) would rank B (2) above A (1)
+    assert best == 3 and tok[1] == A and parent[1] == 0
+    # the whole order-3 continuation (score 3 at every depth) precedes B at depth 1 (score 2)
+    tok, parent, n_valid, _ = OS.draft(ctx, 10)
+    assert tok[1:10].tolist() == [A, 7, Z, B, 8, Z, B, 9, B]
+    assert parent[1:10].tolist() == [0, 1, 2, 3, 4, 5, 6, 7, 0]
+
+
+def test_draft_keeps_at_most_16_candidates_most_recent_first():
+    R = 999
+    follow = list(range(201, 217))                     # B1..B16 after the 16 most recent R
+    ctx = [R, follow[-1], 5]                           # the 17th (oldest) R is also followed by B16
+    for b in reversed(follow):
+        ctx += [R, b, 6]
+    ctx += [777, R]
+    ell = OS.match_lengths(ctx)
+    assert int((ell >= 1).sum()) == 17 and int(ell.max()) == 1
+    tok, parent, n_valid, best = OS.draft(ctx, 2)
+    # cap 16: B16 keeps score 1 and the most recent candidate's B1 comes first; without the
+    # cap B16 would score 2
+    assert best == 1 and tok[1] == follow[0]
+    tok, _, _, _ = OS.draft(ctx, 16)
+    assert tok[1:16].tolist() == follow[:15]          # equal scores: insertion (recency) order
+
+
+def test_draft_ties_prefer_shallow_nodes_then_insertion():
+    R, P, Q, S = 300, 301, 302, 303
+    # two order-1 candidates: the most recent continues P Q, the older one S
+    ctx = [R, S, 9, 9, 9, 9, 9, 9, 9, 9, R, P, Q, 8, 8, 8, 8, 8, 8, 8, 8, R]
+    ell = OS.match_lengths(ctx)
+    assert [p for p in range(len(ctx) - 1) if ell[p] >= 1] == [0, 10] and int(ell.max()) == 1
+    tok, parent, n_valid, _ = OS.draft(ctx, 3)
+    # P (score 1, depth 1, inserted first), then S (score 1, depth 1) before Q (score 1, depth 2)
+    assert tok[1:3].tolist() == [P, S] and parent[1:3].tolist() == [0, 0]
+
+
+def test_draft_score_outranks_depth():
+    R, P, Q, S = 400, 401, 402, 403
+    # an order-2 candidate continues P Q; an order-1 candidate continues S
+    ctx = [7, R, P, Q, 5, 5, 5, 5, 5, 5, 5, 5, 6, R, S, 5, 5, 5, 5, 5, 5, 5, 5, 7, R]
+    ell = OS.match_lengths(ctx)
+    assert ell[1] == 2 and ell[13] == 1
+    tok, parent, n_valid, best = OS.draft(ctx, 3)
+    # Q (score 2, depth 2) before S (score 1, depth 1)
+    assert best == 2 and tok[1:3].tolist() == [P, Q] and parent[1:3].tolist() == [0, 1]
