@@ -122,10 +122,21 @@ w4a8_status w4a8_matmul(const int8_t* a_q, const float* a_s, int M, int K, const
 
 /* Host, synchronous.  Reads the device status word of a matmul workspace (call after the
  * stream has finished).  *flags = 0 if every bounded pipeline wait of the kernels that
- * used this workspace completed; otherwise bit 16 (timeout) is set and the call returns
- * W4A8_ERR_DEVICE_FLAG.  The workspace must be zero-filled once before its first use for
+ * used this workspace completed; otherwise it holds W4A8_FLAG_ERR_TIMEOUT (16) and the call
+ * returns W4A8_ERR_DEVICE_FLAG.  The workspace must be zero-filled once before its first use for
  * this word to be meaningful. */
 w4a8_status w4a8_matmul_check(const void* workspace, int M, int K, int N, uint32_t* flags);
+
+/* Device, test-only fault injection without a fault [P2 "WebGPU for LLM Inference, in depth":
+ * error scopes and device loss -- a failed submission is reported, the device stays usable].
+ * Same arguments as w4a8_matmul; the matmul kernel runs in a variant whose copy warp issues no
+ * copy, so every consumer's bounded wait (shortened to 1 ms) expires: the kernel sets the
+ * workspace status word to W4A8_FLAG_ERR_TIMEOUT (read it with w4a8_matmul_check), leaves y
+ * unwritten, has no copy in flight and returns.  Nothing hangs or faults; later calls on the
+ * same device work normally.  The production kernels are separate instantiations. */
+w4a8_status w4a8_matmul_inject_timeout(const int8_t* a_q, const float* a_s, int M, int K, const uint32_t* w_t,
+                                       const uint16_t* s_t, int N, float* y, void* workspace, size_t workspace_bytes,
+                                       void* stream);
 
 /* Device.  The same product as w4a8_matmul (same kernels, same bits) for callers that
  * cannot allocate device memory -- e.g. code already inside a CUDA stream capture, or hosts
@@ -136,9 +147,18 @@ w4a8_status w4a8_matmul_check(const void* workspace, int M, int K, int N, uint32
  * that first call should come before any stream capture.  All calls share the array and it
  * keeps the last call's contents (each call clears what must start at zero): calls that can
  * overlap on the GPU (different streams, or threads without ordering) race and must not be
- * issued.  The paper has no counterpart of this entry point. */
+ * issued.  A bounded wait inside the kernel that expires leaves y incomplete and sets the
+ * array's status word, which w4a8_matmul_noalloc_check reads.  The paper has no counterpart of
+ * this entry point. */
 w4a8_status w4a8_matmul_noalloc(const int8_t* a_q, const float* a_s, int M, int K, const uint32_t* w_t,
                                 const uint16_t* s_t, int N, float* y, void* stream);
+
+/* Host, synchronous.  The status word of the last w4a8_matmul_noalloc call on the current
+ * device (call after that call's stream has finished; a later call clears it): *flags = 0 if
+ * every bounded pipeline wait of its kernels completed, else W4A8_FLAG_ERR_TIMEOUT (16), y was
+ * left incomplete and the call returns W4A8_ERR_DEVICE_FLAG.  Allocates nothing.  The paper has
+ * no counterpart of this entry point. */
+w4a8_status w4a8_matmul_noalloc_check(uint32_t* flags);
 
 /* Number of K slices S that w4a8_matmul uses for a (K, N) shape (host). */
 int w4a8_matmul_slices(int K, int N);
@@ -238,6 +258,19 @@ w4a8_status w4a8_prefill(w4a8_session* s, const int32_t* prompt, int n, int max_
  * pred[i] = argmax of its logits (lowest index on ties).  logits: optional device
  * fp32 [N][vocab] copy of the logits (NULL = none).  1 <= N <= 16. */
 w4a8_status tree_verify_step(w4a8_session* s, int N, float* logits, void* stream);
+/* Host.  Bytes of the code trace of a verification pass of N tokens (1 <= N <= 16):
+ * N * (n_layers * (2 * hidden + n_heads * head_dim + ffn) + hidden). */
+w4a8_status w4a8_model_trace_bytes(const w4a8_model* m, int N, size_t* bytes);
+/* Device.  tree_verify_step that also writes the int8 activation codes the matmuls consumed
+ * [P1 Small-Batch Verification Kernels: int8 activations quantised right before each matrix
+ * multiplication], for tests and tools: codes (device int8, codes_bytes >= the size from
+ * w4a8_model_trace_bytes) receives, for each layer in order, the codes of the RMSNorm output
+ * before Q/K/V [N][hidden], of the attention output before O [N][n_heads*head_dim], of the
+ * RMSNorm output before gate/up [N][hidden] and of the SwiGLU output before down [N][ffn],
+ * then those of the final RMSNorm output before the LM head [N][hidden].  W4A8_ERR_CAPACITY if
+ * the buffer is too small (nothing is launched). */
+w4a8_status w4a8_tree_verify_trace(w4a8_session* s, int N, float* logits, int8_t* codes, size_t codes_bytes,
+                                   void* stream);
 /* Device.  Greedy acceptance [P1; P3 section 4]: walks from the root following the
  * lowest-index child whose token equals its parent's prediction; commits the accepted
  * drafts and the bonus token (at most max_new - n_generated, stopping after eos); updates
@@ -338,6 +371,12 @@ w4a8_status w4a8_session_get_context(w4a8_session* s, int32_t* out, int cap, int
  * n exceeds the tree's valid nodes.  Overwrites the session's query and attention
  * scratch buffers (tests and tools). */
 w4a8_status w4a8_session_attention(w4a8_session* s, int layer, int n, const float* q, float* out, void* stream);
+/* Device.  The inverse of w4a8_session_copy_kv: writes K and V of one layer, slots
+ * [slot0, slot0+n), from k_in/v_in (device fp32 [n_kv_heads][n][head_dim]) into the cache, e.g.
+ * to restore a saved cache or to verify on a given cache [P1 GPU-Resident Speculation Loop: the
+ * committed KV cache is the state a verification step reads].  The control state is unchanged. */
+w4a8_status w4a8_session_load_kv(w4a8_session* s, int layer, int slot0, int n, const float* k_in, const float* v_in,
+                                 void* stream);
 /* Device.  Copies K and V of one layer, slots [slot0, slot0+n), into k_out/v_out (device
  * fp32 [n_kv_heads][n][head_dim]). */
 w4a8_status w4a8_session_copy_kv(w4a8_session* s, int layer, int slot0, int n, float* k_out, float* v_out,

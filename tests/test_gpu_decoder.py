@@ -2,20 +2,13 @@
 
 The tiny decoder (2 layers, hidden 256, 4/2 heads of 64, FFN 688 padded to 704, vocab
 4096) is built twice from the same seeded stream: on the device by the library's own
-quantiser, and on the host by the oracle's.  Logit tolerance (per row): max |diff| <=
-2e-3 * (max - min of the oracle row); a greedy token must match wherever the oracle's
-top-2 margin exceeds twice that bound.
-
-Requantisation makes the logits sensitive to the last bit of the values that feed an
-int8 decision: once one code differs by one step, the difference reaches every later
-position through the KV cache (evaluating the same definition in fp32 instead of fp64,
-without any GPU, moves the logits after the 64-token prompt by up to 0.8% of their
-range).  The oracle records, for every token, the distance of its closest int8 decision
-to a rounding boundary.  A row must meet the 2e-3 bound whenever every decision in its
-dependency cone (the cached context and its ancestors) is at least DELTA = 2e-3 code units
-from a boundary -- far beyond the fp32 rounding of the kernels, so no code can differ;
-otherwise it must stay within 2e-2 of the range and its greedy token must agree where the
-margin allows.
+quantiser, and on the host by the oracle's.  Logits are compared at the code level
+(``tests/parity.py``): a row whose dependency cone holds no int8 code that differs from the
+oracle's must meet the north-star bound max |diff| <= 2e-3 * (max - min of the oracle row);
+every first differing code must be a one-step change at a decision within 2e-3 code units of
+its rounding boundary; rows downstream of such a flip are held to 2e-2; a greedy token must
+match wherever the oracle's top-2 margin exceeds twice the row's bound.  Each group of tests
+asserts that most rows ran at the 2e-3 bound.
 """
 import numpy as np
 import pytest
@@ -29,13 +22,13 @@ from w4a8_verify_gb300 import models as WM
 from oracle import model as OM
 from oracle import spec as OS
 
+import parity as P
+
 pytestmark = pytest.mark.gpu
 
 SHAPE = synth.TINY
 SEED = 1000
-REL_TOL = 2e-3
-REL_TOL_NEAR = 2e-2
-DELTA = 2e-3
+TALLY = P.Tally()
 
 
 def _fill(shape, seed):
@@ -56,6 +49,23 @@ def gpu_model(shape=SHAPE, seed=SEED):
                           shape.vocab, shape.tied, _fill(shape, seed), shape.rms_eps, shape.rope_base)
 
 
+def _oracle_greedy(ow, prompt, max_new):
+    """Plain greedy decoding by the oracle, keeping its model (cache and recorded codes)."""
+    prompt = [int(t) for t in prompt]
+    n = len(prompt)
+    m = OM.Model(ow, n + max_new + 1, record=True)
+    m.prefill(prompt[:-1], head=False)
+    L, tok = n - 1, prompt[-1]
+    out, logits = [], []
+    for _ in range(max_new):
+        lg = m.step(tok, L)
+        logits.append(lg)
+        tok = OM.argmax_lowest(lg)
+        out.append(tok)
+        L += 1
+    return out, logits, m
+
+
 @pytest.fixture(scope="module")
 def tiny():
     if not torch.cuda.is_available():
@@ -65,8 +75,9 @@ def tiny():
     m = gpu_model()
     ow = OM.build_weights(SHAPE, SEED)
     prompt = synth.motif_prompt(1001, 64, 4, 16, 0.1, SHAPE.vocab)
-    greedy, glogits = OM.greedy_decode(ow, prompt, 32)
-    return dict(model=m, ow=ow, prompt=prompt, greedy=greedy, glogits=glogits)
+    greedy, glogits, gm = _oracle_greedy(ow, prompt, 32)
+    yield dict(model=m, ow=ow, prompt=prompt, greedy=greedy, glogits=glogits, gmodel=gm)
+    print("\n[tiny decoder parity] " + TALLY.summary())
 
 
 def _session(t, kv_cap=256, ctx_cap=512, max_window=16, eos=-1):
@@ -77,56 +88,38 @@ def _dev(a, dtype=torch.int32):
     return torch.as_tensor(np.asarray(a), dtype=dtype).cuda()
 
 
-def _check_rows(gpu, ref, pred=None, rel=REL_TOL, near=None):
-    """Per-row tolerance and greedy-token agreement.  near[i]: row i depends on an int8
-    decision within DELTA of a rounding boundary (looser bound)."""
-    for i in range(ref.shape[0]):
-        rng = ref[i].max() - ref[i].min()
-        bound = (REL_TOL_NEAR if near is not None and near[i] else rel) * rng
-        err = np.abs(gpu[i].astype(np.float64) - ref[i]).max()
-        assert err <= bound, (i, err, bound)
-        if pred is not None:
-            top2 = np.sort(ref[i])[-2:]
-            if top2[1] - top2[0] > 2 * bound:
-                assert pred[i] == int(np.argmax(ref[i])), i
-
-
-def _forced_sequential_logits(t, tokens):
-    """GPU single-token steps over `tokens` (teacher-forced): logits after each token."""
-    s = _session(t)
-    s.prefill(_dev(tokens[:1]), max_new=len(tokens) + 4)
-    V = SHAPE.vocab
-    out = []
-    lg = torch.empty((1, V), dtype=torch.float32, device="cuda")
-    for j, tok in enumerate(tokens):
-        s.set_tree([int(tok)], [-1])
-        s.tree_verify_step(1, lg)
-        out.append(lg[0].clone())
-        s.accept_greedy(1)   # commits the root's K/V (L_c += 1)
-    torch.cuda.synchronize()
-    return torch.stack(out), s
-
-
 # ------------------------------------------------------------------------------ verify
 
+@pytest.mark.parametrize("seed,N,L", [(0, 16, 200), (1, 8, 7), (2, 5, 15), (3, 1, 191), (4, 2, 8), (5, 16, 63),
+                                      (6, 11, 64), (7, 16, 0), (8, 16, 129), (9, 3, 1)])
+def test_tree_verify_on_given_cache_matches_oracle(tiny, seed, N, L):
+    rng = np.random.default_rng(seed)
+    tok, parent = synth.random_tree(rng, N, SHAPE.vocab)
+    s = _session(tiny)
+    s.prefill(_dev(synth.motif_prompt(3000 + seed, L + 1, 4, 8, 0.1, SHAPE.vocab)), max_new=8)
+    P.verify_on_given_cache(s, tiny["ow"], SHAPE, L, tok, parent, 4000 + seed, TALLY)
+
+
 def _verify_case(tiny, prompt, tok, parent):
+    """Verification after each side's own prefill of the prompt; the context is clean where
+    the GPU's cached K/V equal the oracle's."""
     N = len(tok)
     s = _session(tiny)
     s.prefill(_dev(prompt), max_new=8)
     s.set_tree(tok.tolist(), parent.tolist())
-    lg = torch.empty((N, SHAPE.vocab), dtype=torch.float32, device="cuda")
-    s.tree_verify_step(N, lg)
-    pred = s.pred(N)
     L = len(prompt) - 1
-    m = OM.Model(tiny["ow"], len(prompt) + N + 1)
+    m = OM.Model(tiny["ow"], len(prompt) + N + 1, record=True)
     if L > 0:
-        m.prefill(list(prompt[:-1]))
+        m.prefill(list(prompt[:-1]), head=False)
+    ctx_ok = P.ctx_clean(s, SHAPE, m, L)
+    lg, codes, pred = P.traced_verify(s, SHAPE, N)
     ref = OS.tree_verify(m, L, tok, parent)
-    ctx_margin = m.margin[:L].min() if L > 0 else np.inf
-    near = [min(ctx_margin, min(m.margin[L + a] for a in OS.ancestors_or_self(parent, i))) < DELTA
-            for i in range(N)]
-    _check_rows(lg.cpu().numpy(), ref, pred, REL_TOL, near)
-    return sum(near)
+    fl = P.Flips(codes, m.record, SHAPE, L, parent)
+    ff = fl.check_first_flips() if ctx_ok else []
+    clean = [ctx_ok and fl.row_clean(i) for i in range(N)]
+    st, lo = P.check_rows(lg, ref, pred, clean)
+    TALLY.add(st, lo, ff)
+    return st, lo
 
 
 @pytest.mark.parametrize("seed,N,plen", [(0, 16, 32), (1, 8, 8), (2, 5, 16), (3, 1, 32), (4, 2, 9), (5, 16, 24),
@@ -143,6 +136,54 @@ def test_tree_verify_matches_oracle_after_64_token_prompt(tiny, seed, N):
     rng = np.random.default_rng(seed)
     tok, parent = synth.random_tree(rng, N, SHAPE.vocab)
     _verify_case(tiny, tiny["prompt"], tok, parent)
+
+
+def test_teacher_forced_steps_match_oracle_greedy(tiny):
+    """Single-token GPU steps fed the oracle's greedy tokens: every step's logits against the
+    oracle's (no cascade after an allowed token disagreement)."""
+    prompt = [int(t) for t in tiny["prompt"]]
+    greedy, glogits, gm = tiny["greedy"], tiny["glogits"], tiny["gmodel"]
+    s = _session(tiny)
+    s.prefill(_dev(prompt), max_new=len(greedy) + 4)
+    L0 = len(prompt) - 1
+    strict = loose = 0
+    for j, tok in enumerate([prompt[-1]] + greedy[:-1]):
+        L = L0 + j
+        s.set_tree([int(tok)], [-1])
+        lg, codes, pred = P.traced_verify(s, SHAPE, 1)
+        ctx_ok = P.ctx_clean(s, SHAPE, gm, L)
+        fl = P.Flips(codes, {(L, st): gm.record[(L, st)] for st in OM.stage_names(SHAPE.n_layers)}, SHAPE, L, [-1])
+        ff = fl.check_first_flips() if ctx_ok else []
+        clean = [ctx_ok and fl.row_clean(0)]
+        a, b = P.check_rows(lg, glogits[j][None, :], pred, clean)
+        TALLY.add(a, b, ff)
+        strict += a
+        loose += b
+        s.accept_greedy(1)      # commits the step's K/V (the next root is set explicitly)
+    assert strict >= loose, (strict, loose)
+
+
+def test_most_rows_at_the_north_star_bound(tiny):
+    """Runs after the parity tests of this module: most rows were held to 2e-3."""
+    if TALLY.strict + TALLY.loose == 0:
+        pytest.skip("no parity rows ran in this session (test selection)")
+    assert TALLY.strict > TALLY.loose, TALLY.summary()
+
+
+def _forced_sequential_logits(t, tokens):
+    """GPU single-token steps over `tokens` (teacher-forced): logits after each token."""
+    s = _session(t)
+    s.prefill(_dev(tokens[:1]), max_new=len(tokens) + 4)
+    V = SHAPE.vocab
+    out = []
+    lg = torch.empty((1, V), dtype=torch.float32, device="cuda")
+    for j, tok in enumerate(tokens):
+        s.set_tree([int(tok)], [-1])
+        s.tree_verify_step(1, lg)
+        out.append(lg[0].clone())
+        s.accept_greedy(1)   # commits the root's K/V (L_c += 1)
+    torch.cuda.synchronize()
+    return torch.stack(out), s
 
 
 def test_verify_n_nodes_bitwise_equals_single_steps(tiny):
@@ -163,6 +204,38 @@ def test_verify_n_nodes_bitwise_equals_single_steps(tiny):
         seq, _ = _forced_sequential_logits(tiny, prompt[:-1] + [int(tok[j]) for j in path])
         for depth, node in enumerate(path):
             assert torch.equal(lg[node], seq[len(prompt) - 1 + depth]), (leaf, node)
+
+
+def test_trace_does_not_change_the_pass(tiny):
+    """The traced pass computes the same logits, bit for bit, as the plain one."""
+    prompt = list(tiny["prompt"])
+    tok, parent = synth.random_tree(np.random.default_rng(3), 9, SHAPE.vocab)
+    out = []
+    for traced in (False, True):
+        s = _session(tiny)
+        s.prefill(_dev(prompt), max_new=8)
+        s.set_tree(tok.tolist(), parent.tolist())
+        if traced:
+            out.append(P.traced_verify(s, SHAPE, 9)[0])
+        else:
+            lg = torch.empty((9, SHAPE.vocab), dtype=torch.float32, device="cuda")
+            s.tree_verify_step(9, lg)
+            out.append(lg.cpu().numpy())
+    assert np.array_equal(out[0], out[1])
+
+
+def test_load_kv_round_trip(tiny):
+    s = _session(tiny)
+    s.prefill(_dev(list(tiny["prompt"])), max_new=8)
+    ks, vs = P.synthetic_kv(SHAPE, 77, 40)
+    s.load_kv(1, 5, 40, torch.from_numpy(ks[0]).cuda(), torch.from_numpy(vs[0]).cuda())
+    k = torch.empty((SHAPE.n_kv_heads, 40, SHAPE.head_dim), dtype=torch.float32, device="cuda")
+    v = torch.empty_like(k)
+    s.copy_kv(1, 5, 40, k, v)
+    torch.cuda.synchronize()
+    assert np.array_equal(k.cpu().numpy(), ks[0]) and np.array_equal(v.cpu().numpy(), vs[0])
+    with pytest.raises(W.W4A8Error):
+        s.load_kv(0, 250, 40, k, v)                     # past kv_cap
 
 
 def test_prefill_kv_bitwise_equals_sequential_kv(tiny):
@@ -238,6 +311,13 @@ def test_speculative_equals_greedy_on_gpu(tiny, N, Wn):
     assert spec == greedy
     assert rep.n_tokens == 32 and rep.flags & W.FLAG_TERMINATED
     assert 1 <= 32 / rep.n_steps <= min(N, 9)
+    if N >= 4:
+        # multi-node acceptance and compaction are exercised: drafts were accepted, and where
+        # the GPU's greedy tokens are the oracle's, the step count is the oracle loop's
+        assert rep.n_steps < 32 and rep.accepted_drafts >= 32 - rep.n_steps
+        if greedy == tiny["greedy"]:
+            _, o_stats = OS.spec_decode(tiny["ow"], prompt, 32, N)
+            assert rep.n_steps == len(o_stats)
 
 
 def test_gpu_greedy_matches_oracle_greedy(tiny):
@@ -248,7 +328,7 @@ def test_gpu_greedy_matches_oracle_greedy(tiny):
     for i, (a, b) in enumerate(zip(out, ref)):
         if a != b:
             top2 = np.sort(lg[i])[-2:]
-            assert top2[1] - top2[0] <= 2 * REL_TOL * (lg[i].max() - lg[i].min()), i
+            assert top2[1] - top2[0] <= 2 * P.REL_TOL * (lg[i].max() - lg[i].min()), i
             break
 
 

@@ -69,8 +69,10 @@ _SIGNATURES = {
     "w4a8_matmul_workspace_bytes": [_i32, _i32, _i32, _c.POINTER(_sz)],
     "w4a8_matmul": [_vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp],
     "w4a8_matmul_slices": [_i32, _i32],
+    "w4a8_matmul_inject_timeout": [_vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp],
     "w4a8_matmul_check": [_vp, _i32, _i32, _i32, _c.POINTER(_c.c_uint32)],
     "w4a8_matmul_noalloc": [_vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp],
+    "w4a8_matmul_noalloc_check": [_c.POINTER(_c.c_uint32)],
     "w4a8_model_create": [_c.POINTER(ModelDesc), _c.POINTER(_vp)],
     "w4a8_model_load_tensor": [_vp, _i32, _i32, _vp, _vp, _vp],
     "w4a8_model_weight_bytes": [_vp, _c.POINTER(_sz)],
@@ -79,6 +81,8 @@ _SIGNATURES = {
     "w4a8_session_destroy": [_vp],
     "w4a8_prefill": [_vp, _vp, _i32, _i32, _vp],
     "tree_verify_step": [_vp, _i32, _vp, _vp],
+    "w4a8_model_trace_bytes": [_vp, _i32, _c.POINTER(_sz)],
+    "w4a8_tree_verify_trace": [_vp, _i32, _vp, _vp, _sz, _vp],
     "accept_greedy": [_vp, _i32, _vp],
     "kv_compact": [_vp, _vp],
     "ngram_draft": [_vp, _vp],
@@ -100,6 +104,7 @@ _SIGNATURES = {
     "w4a8_session_get_pred": [_vp, _c.POINTER(_i32), _i32],
     "w4a8_session_get_context": [_vp, _c.POINTER(_i32), _i32, _c.POINTER(_i32)],
     "w4a8_session_copy_kv": [_vp, _i32, _i32, _i32, _vp, _vp, _vp],
+    "w4a8_session_load_kv": [_vp, _i32, _i32, _i32, _vp, _vp, _vp],
     "w4a8_session_attention": [_vp, _i32, _i32, _vp, _vp, _vp],
     "w4a8_controller_create": [_c.POINTER(_i32), _c.POINTER(_f32), _i32, _c.POINTER(_vp)],
     "w4a8_controller_destroy": [_vp],
@@ -237,6 +242,24 @@ def w4a8_matmul_noalloc(a_q, a_s, w_t, s_t, N, y, stream=None):
     return y
 
 
+def w4a8_matmul_inject_timeout(a_q, a_s, w_t, s_t, N, y, workspace, stream=None):
+    """Test-only: the matmul with a copy warp that issues nothing, so that its bounded waits
+    expire and the workspace status word reports the timeout (w4a8_matmul_inject_timeout)."""
+    M, K = a_q.shape
+    _call("w4a8_matmul_inject_timeout", _ptr(a_q), _ptr(a_s), M, K, _ptr(w_t), _ptr(s_t), N, _ptr(y),
+          _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def w4a8_matmul_noalloc_check():
+    """Status word of the last w4a8_matmul_noalloc call on the current device (0 = every
+    bounded wait completed; synchronous: call after that stream has finished)."""
+    f = _c.c_uint32()
+    st = lib().w4a8_matmul_noalloc_check(_c.byref(f))
+    if st not in (0, 7):
+        raise W4A8Error("w4a8_matmul_noalloc_check", st)
+    return f.value
+
+
 def w4a8_matmul(a_q, a_s, w_t, s_t, N, y=None, workspace=None, stream=None):
     import torch
     M, K = a_q.shape
@@ -315,6 +338,17 @@ class Session:
 
     def tree_verify_step(self, N, logits=None, stream=None):
         _call("tree_verify_step", self.h, int(N), _ptr(logits), _stream(stream))
+
+    def trace_bytes(self, N):
+        n = _sz()
+        _call("w4a8_model_trace_bytes", self.model.h, int(N), _c.byref(n))
+        return n.value
+
+    def tree_verify_trace(self, N, codes, logits=None, stream=None):
+        """tree_verify_step that also writes the int8 codes of every quantisation point into
+        the device int8 buffer ``codes`` (w4a8_tree_verify_trace)."""
+        _call("w4a8_tree_verify_trace", self.h, int(N), _ptr(logits), _ptr(codes),
+              codes.numel() * codes.element_size(), _stream(stream))
 
     def accept_greedy(self, N, stream=None):
         _call("accept_greedy", self.h, int(N), _stream(stream))
@@ -416,6 +450,10 @@ class Session:
 
     def copy_kv(self, layer, slot0, n, k_out, v_out, stream=None):
         _call("w4a8_session_copy_kv", self.h, int(layer), int(slot0), int(n), _ptr(k_out), _ptr(v_out),
+              _stream(stream))
+
+    def load_kv(self, layer, slot0, n, k_in, v_in, stream=None):
+        _call("w4a8_session_load_kv", self.h, int(layer), int(slot0), int(n), _ptr(k_in), _ptr(v_in),
               _stream(stream))
 
     def attention(self, layer, n, q, out, stream=None):

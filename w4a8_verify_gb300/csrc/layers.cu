@@ -330,6 +330,32 @@ __global__ void __launch_bounds__(512)
   }
 }
 
+// ------------------------------------------------------------------------- code trace
+
+// The int8 codes held by the activation records of M tokens over K inputs (the input of the
+// next matmul), one thread per (token, input), written to out[t][K].  A record holds each code
+// a as the f16 a, or a/16 for the inputs 8..15 and 24..31 of a group (layout.cuh).
+__global__ void k_trace_codes(const uint8_t* __restrict__ act, int M, int K, int8_t* __restrict__ out) {
+  griddep_enter();
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= M * K) return;
+  const int t = idx / K, k = idx - t * K;
+  const int NT = act_tiles(M);
+  const int g = k >> 5, kin = k & 31, p = kin >> 3, tig = (kin & 7) >> 1, h = kin & 1;
+  const int nt = t >> 3, gid = t & 7;
+  const uint8_t* frag = act + (size_t)(g >> 1) * act_rec_bytes(NT) + (nt * 2 + (g & 1)) * 512;
+  const uint32_t w = reinterpret_cast<const uint32_t*>(frag + (gid * 4 + tig) * 16)[p];
+  const unsigned short bits = (unsigned short)(h ? (w >> 16) : (w & 0xffffu));
+  float a = __half2float(__ushort_as_half(bits));
+  if (p & 1) a *= 16.0f;
+  out[(size_t)t * K + k] = (int8_t)__float2int_rn(a);
+}
+
+cudaError_t launch_trace_codes(const DecoderBufs& b, int M, int K, int8_t* out, cudaStream_t st) {
+  const int n = M * K;
+  return launch_pdl(k_trace_codes, dim3((n + 255) / 256), dim3(256), 0, st, (const uint8_t*)b.act, M, K, out);
+}
+
 // ------------------------------------------------------------------------- launchers
 
 size_t attn_smem_bytes(int D, int Nq) { return attn_layout(D, Nq).total; }

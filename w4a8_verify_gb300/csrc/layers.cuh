@@ -26,6 +26,9 @@ cudaError_t launch_swiglu_quant(const DecoderBufs& b, const ModelDims& m, int N,
 // stored to b.logits)
 cudaError_t launch_argmax(const DecoderBufs& b, const ModelDims& m, int N, int lm_S, cudaStream_t st);
 
+// int8 codes of the current activation records (M tokens, K inputs) -> out [M][K]
+cudaError_t launch_trace_codes(const DecoderBufs& b, int M, int K, int8_t* out, cudaStream_t st);
+
 // spec.cu
 cudaError_t launch_accept(const DecoderBufs& b, int N, int window_slot, cudaStream_t st);
 cudaError_t launch_compact(const DecoderBufs& b, const ModelDims& m, cudaStream_t st);

@@ -139,7 +139,16 @@ __global__ void k_window_close(const SpecCtl* ctl, const StepStats* ws, const in
   for (int i = t; i < W * kMaxWidth; i += blockDim.x) to[i] = wt[i];
 }
 
-cudaError_t forward(w4a8_session* s, int N, bool head, float* logits_out, cudaStream_t st) {
+// Bytes of the code trace of one verification pass of N tokens: per layer the codes of the
+// four quantisation points (RMSNorm -> QKV, attention -> O, RMSNorm -> gate|up, SwiGLU -> down),
+// then the final RMSNorm -> LM head, each [N][inputs].
+size_t trace_bytes(const ModelDims& d, int N) {
+  return (size_t)N * ((size_t)d.n_layers * (2 * d.H + d.Hq * d.D + d.F) + d.H);
+}
+
+// trace: optional device buffer of trace_bytes(d, N) bytes receiving the int8 codes of every
+// quantisation point (tests and tools; not used by the decoding loop).
+cudaError_t forward(w4a8_session* s, int N, bool head, float* logits_out, cudaStream_t st, int8_t* trace = nullptr) {
   const DecoderBufs& b = s->b;
   w4a8_model* m = s->m;
   const ModelDims& d = m->d;
@@ -149,18 +158,29 @@ cudaError_t forward(w4a8_session* s, int N, bool head, float* logits_out, cudaSt
   // folds: RoPE/KV, the residual update before RMSNorm, SwiGLU.
   const float* res = nullptr;
   int res_S = 0;
+  int8_t* tr = trace;
+  auto trace_codes = [&](int K) -> cudaError_t {
+    if (!tr) return cudaSuccess;
+    cudaError_t e = launch_trace_codes(b, N, K, tr, st);
+    tr += (size_t)N * K;
+    return e;
+  };
   for (int l = 0; l < d.n_layers; ++l) {
     TRYC(launch_rmsnorm_quant(b, d, N, res, res_S, st));
+    TRYC(trace_codes(d.H));
     TRYC(mm_run(m->p_qkv, m->qkv_w[l], m->qkv_s[l], b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets,
                 flags, flags, st));
     TRYC(launch_rope_kv(b, d, N, l, m->p_qkv.S, st));
     TRYC(launch_attention(b, d, N, l, st));
+    TRYC(trace_codes(d.Hq * d.D));
     TRYC(mm_run(m->p_o, m->o_w[l], m->o_s[l], b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets, flags,
                 flags, st));
     TRYC(launch_rmsnorm_quant(b, d, N, b.mm_part, m->p_o.S, st));
+    TRYC(trace_codes(d.H));
     TRYC(mm_run(m->p_gu, m->gu_w[l], m->gu_s[l], b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets,
                 flags, flags, st));
     TRYC(launch_swiglu_quant(b, d, N, m->p_gu.S, st));
+    TRYC(trace_codes(d.F));
     TRYC(mm_run(m->p_dn, m->dn_w[l], m->dn_s[l], b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets,
                 flags, flags, st));
     res = b.mm_part;
@@ -168,6 +188,7 @@ cudaError_t forward(w4a8_session* s, int N, bool head, float* logits_out, cudaSt
   }
   if (head) {
     TRYC(launch_rmsnorm_quant(b, d, N, res, res_S, st));
+    TRYC(trace_codes(d.H));
     TRYC(mm_run(m->p_lm, m->lm_w, m->lm_s, b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets, flags,
                 flags, st));
     TRYC(launch_argmax(b, d, N, m->p_lm.S, st));
@@ -415,6 +436,20 @@ W4A8_API w4a8_status w4a8_prefill(w4a8_session* s, const int32_t* prompt, int n,
 W4A8_API w4a8_status tree_verify_step(w4a8_session* s, int N, float* logits, void* stream) {
   if (!s || N < 1 || N > kMaxWidth) return W4A8_ERR_ARG;
   W4A8_CUDA_TRY(forward(s, N, true, logits, as_stream(stream)));
+  return W4A8_OK;
+}
+
+W4A8_API w4a8_status w4a8_model_trace_bytes(const w4a8_model* m, int N, size_t* bytes) {
+  if (!m || !bytes || N < 1 || N > kMaxWidth) return W4A8_ERR_ARG;
+  *bytes = trace_bytes(m->d, N);
+  return W4A8_OK;
+}
+
+W4A8_API w4a8_status w4a8_tree_verify_trace(w4a8_session* s, int N, float* logits, int8_t* codes, size_t codes_bytes,
+                                            void* stream) {
+  if (!s || !codes || N < 1 || N > kMaxWidth) return W4A8_ERR_ARG;
+  if (codes_bytes < trace_bytes(s->m->d, N)) return W4A8_ERR_CAPACITY;
+  W4A8_CUDA_TRY(forward(s, N, true, logits, as_stream(stream), codes));
   return W4A8_OK;
 }
 
@@ -870,6 +905,22 @@ W4A8_API w4a8_status w4a8_session_attention(w4a8_session* s, int layer, int n, c
   W4A8_CUDA_TRY(cudaMemcpyAsync(s->b.qrot, q, qn * 4, cudaMemcpyDeviceToDevice, cs));
   W4A8_CUDA_TRY(launch_tree_attention(s->b, d, n, layer, cs));
   W4A8_CUDA_TRY(cudaMemcpyAsync(out, s->b.qkv, qn * 4, cudaMemcpyDeviceToDevice, cs));
+  return W4A8_OK;
+}
+
+W4A8_API w4a8_status w4a8_session_load_kv(w4a8_session* s, int layer, int slot0, int n, const float* k_in,
+                                          const float* v_in, void* stream) {
+  if (!s || !k_in || !v_in || layer < 0 || layer >= s->m->d.n_layers || slot0 < 0 || n < 1 ||
+      slot0 + n > s->b.kv_cap)
+    return W4A8_ERR_ARG;
+  const ModelDims& d = s->m->d;
+  cudaStream_t cs = as_stream(stream);
+  for (int h = 0; h < d.Hkv; ++h) {
+    const size_t dst = (((size_t)layer * d.Hkv + h) * s->b.kv_cap + slot0) * d.D;
+    const size_t src = (size_t)h * n * d.D;
+    W4A8_CUDA_TRY(cudaMemcpyAsync(s->b.kcache + dst, k_in + src, (size_t)n * d.D * 4, cudaMemcpyDeviceToDevice, cs));
+    W4A8_CUDA_TRY(cudaMemcpyAsync(s->b.vcache + dst, v_in + src, (size_t)n * d.D * 4, cudaMemcpyDeviceToDevice, cs));
+  }
   return W4A8_OK;
 }
 
