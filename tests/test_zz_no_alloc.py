@@ -44,6 +44,7 @@ def test_noalloc_matches_workspace_entry_point_twice(M, K, N):
         W.w4a8_matmul_noalloc(a_q, a_s, w_t, s_t, N, y)
         torch.cuda.synchronize()
         assert torch.equal(y, ref)
+        assert W.w4a8_matmul_noalloc_check() == 0        # no bounded wait expired
 
 
 def test_noalloc_alternating_shapes():

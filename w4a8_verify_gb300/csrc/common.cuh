@@ -113,12 +113,12 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 // Bounded wait: gives up after kWaitLimitNs and reports false.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (unsigned it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if ((it & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 // TMA tiled copy of one 4-D box (coordinates innermost first) of `map` into shared memory;

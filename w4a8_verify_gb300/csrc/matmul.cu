@@ -155,7 +155,14 @@ __device__ __forceinline__ void mm_chunks(const uint8_t* stage, int u0, int rl0,
 // griddepcontrol.wait (weights are constant), activations only after it.  A unit's result is
 // folded with the other slices of its row group by the last unit to finish (ticket), in
 // ascending slice order.
-template <int NT>
+// Wait limit of the test-only variant below (FAULT): its producer issues no copies, so every
+// consumer wait runs out after this long.
+constexpr uint64_t kFaultWaitNs = 1000000ull;
+
+// FAULT (test-only instantiation, never used by the decoder or w4a8_matmul): the producer
+// issues no copy and the consumers' bounded waits use kFaultWaitNs, so the timeout path (status
+// flag, skipped output, no copy left in flight) runs without any fault or hang.
+template <int NT, bool FAULT>
 __global__ void __launch_bounds__(kMmThreads)
     k_mm(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ st, const uint8_t* __restrict__ act,
          const float* __restrict__ a_s, int M, int N, int ldy, int KC, int cps, int S, float* __restrict__ y,
@@ -232,6 +239,7 @@ __global__ void __launch_bounds__(kMmThreads)
       Pos pro[kStages];
       int npro = 0;
       Pos ps{(int)blockIdx.x, 0};
+      if (FAULT) ps.w = units;  // nothing is issued
       while (npro < kStages && ps.w < units) {
         issue_weights(ps, npro);
         pro[npro++] = ps;
@@ -284,7 +292,7 @@ __global__ void __launch_bounds__(kMmThreads)
           for (int e = 0; e < 4; ++e) acc[r][nt][e] = 0.0f;
       for (int b = 0; b < nb; ++b, ++it) {
         const int stg = it % kStages;
-        if (ok && !mbar_wait(&full[stg], (it / kStages) & 1)) {
+        if (ok && !mbar_wait(&full[stg], (it / kStages) & 1, FAULT ? kFaultWaitNs : kWaitLimitNs)) {
           if (lane == 0) atomicOr(err, FLAG_ERR_TIMEOUT);
           ok = false;
         }
@@ -408,9 +416,13 @@ __global__ void __launch_bounds__(kMmThreads)
 }
 
 cudaError_t mm_configure() {
-  cudaError_t e = cudaFuncSetAttribute(k_mm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmSmem);
+  cudaError_t e = cudaFuncSetAttribute(k_mm<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmSmem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_mm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmSmem);
+  e = cudaFuncSetAttribute(k_mm<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_mm<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_mm<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmSmem);
 }
 
 cudaError_t mm_run(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, const uint8_t* act, const float* a_s,
@@ -424,11 +436,31 @@ cudaError_t mm_run(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, 
   const uint8_t* w8 = reinterpret_cast<const uint8_t*>(wt);
   const uint8_t* s8 = reinterpret_cast<const uint8_t*>(st);
   if (act_tiles(M) == 1)
-    return launch_pdl(k_mm<1>, grid, block, kMmSmem, stream, w8, s8, act, a_s, M, p.N, ldy, p.KC, p.cps, p.S, y,
-                      epi, part, tickets, err, stop);
-  return launch_pdl(k_mm<2>, grid, block, kMmSmem, stream, w8, s8, act, a_s, M, p.N, ldy, p.KC, p.cps, p.S, y, epi,
-                    part, tickets, err, stop);
+    return launch_pdl(k_mm<1, false>, grid, block, kMmSmem, stream, w8, s8, act, a_s, M, p.N, ldy, p.KC, p.cps, p.S,
+                      y, epi, part, tickets, err, stop);
+  return launch_pdl(k_mm<2, false>, grid, block, kMmSmem, stream, w8, s8, act, a_s, M, p.N, ldy, p.KC, p.cps, p.S, y,
+                    epi, part, tickets, err, stop);
 }
+
+namespace {
+// The test-only FAULT variant with the launch of mm_run (EPI_STORE).
+cudaError_t mm_run_fault(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, const uint8_t* act,
+                         const float* a_s, int M, float* y, float* part, unsigned* tickets, unsigned* err,
+                         cudaStream_t stream) {
+  static cudaError_t configured = mm_configure();
+  if (configured != cudaSuccess) return configured;
+  const long long units = (long long)p.n_rg * p.S;
+  dim3 grid((unsigned)(units < kPersistentCtas ? units : kPersistentCtas));
+  const uint8_t* w8 = reinterpret_cast<const uint8_t*>(wt);
+  const uint8_t* s8 = reinterpret_cast<const uint8_t*>(st);
+  const unsigned* no_stop = nullptr;
+  if (act_tiles(M) == 1)
+    return launch_pdl(k_mm<1, true>, grid, dim3(kMmThreads), kMmSmem, stream, w8, s8, act, a_s, M, p.N, p.N, p.KC,
+                      p.cps, p.S, y, (int)EPI_STORE, part, tickets, err, no_stop);
+  return launch_pdl(k_mm<2, true>, grid, dim3(kMmThreads), kMmSmem, stream, w8, s8, act, a_s, M, p.N, p.N, p.KC,
+                    p.cps, p.S, y, (int)EPI_STORE, part, tickets, err, no_stop);
+}
+}  // namespace
 
 // One warp per (chunk, group, 8-token tile): lane (gid, tig) builds its f16 fragment word
 // of token 8*nt + gid and the group sums that seed the accumulators.
@@ -534,6 +566,26 @@ W4A8_API w4a8_status w4a8_matmul(const int8_t* a_q, const float* a_s, int M, int
   cudaStream_t st = as_stream(stream);
   W4A8_CUDA_TRY(act_prep_run(a_q, M, K, K, act, tickets, p.n_rg, st));
   W4A8_CUDA_TRY(mm_run(p, w_t, s_t, act, a_s, M, y, N, EPI_STORE, part, tickets, err, nullptr, st));
+  return W4A8_OK;
+}
+
+W4A8_API w4a8_status w4a8_matmul_inject_timeout(const int8_t* a_q, const float* a_s, int M, int K,
+                                                const uint32_t* w_t, const uint16_t* s_t, int N, float* y,
+                                                void* workspace, size_t workspace_bytes, void* stream) {
+  if (!a_q || !a_s || !w_t || !s_t || !y || !workspace || M <= 0 || K <= 0 || N <= 0) return W4A8_ERR_ARG;
+  if (M > 16 || K % 32 || N % 16) return W4A8_ERR_SHAPE;
+  if (!aligned(w_t, 16) || !aligned(s_t, 16) || !aligned(workspace, 256) || !aligned(a_q, 4) || !aligned(a_s, 4))
+    return W4A8_ERR_ARG;
+  const MatmulPlan p = mm_plan(K, N);
+  const MatmulWorkspace w = ws_layout(p);
+  if (workspace_bytes < w.total) return W4A8_ERR_CAPACITY;
+  char* base = static_cast<char*>(workspace);
+  cudaStream_t st = as_stream(stream);
+  unsigned* tickets = reinterpret_cast<unsigned*>(base + w.off_tickets);
+  W4A8_CUDA_TRY(act_prep_run(a_q, M, K, K, reinterpret_cast<uint8_t*>(base + w.off_act), tickets, p.n_rg, st));
+  W4A8_CUDA_TRY(mm_run_fault(p, w_t, s_t, reinterpret_cast<uint8_t*>(base + w.off_act), a_s, M, y,
+                             reinterpret_cast<float*>(base + w.off_part), tickets,
+                             reinterpret_cast<unsigned*>(base + w.off_err), st));
   return W4A8_OK;
 }
 

@@ -50,22 +50,32 @@ W4A8_API w4a8_status w4a8_matmul_noalloc(const int8_t* a_q, const float* a_s, in
   if (M > 16 || K % 32 || N % 16) return W4A8_ERR_SHAPE;
   if (!aligned(w_t, 16) || !aligned(s_t, 16) || !aligned(a_q, 4) || !aligned(a_s, 4)) return W4A8_ERR_ARG;
   const MatmulPlan p = mm_plan(K, N);
-  // [activation records][split-K partials][n_rg slice counters, status word]
-  const size_t off_part = align256(act_bytes(K));
-  const size_t off_tickets = align256(off_part + p.part_floats * 4);
-  const size_t total = off_tickets + ((size_t)p.n_rg + 1) * 4;
+  // [status word, n_rg slice counters][activation records][split-K partials]: the status word
+  // sits at offset 0 for every shape, so that w4a8_matmul_noalloc_check can find it
+  const size_t off_act = align256(((size_t)p.n_rg + 1) * 4);
+  const size_t off_part = align256(off_act + act_bytes(K));
+  const size_t total = off_part + p.part_floats * 4;
   if (total > kStaticScratchBytes) return W4A8_ERR_CAPACITY;
   void* base_v = nullptr;
   const w4a8_status st = scratch_address(&base_v);
   if (st != W4A8_OK) return st;
   char* base = static_cast<char*>(base_v);
-  uint8_t* act = reinterpret_cast<uint8_t*>(base);
+  unsigned* status = reinterpret_cast<unsigned*>(base);
+  uint8_t* act = reinterpret_cast<uint8_t*>(base + off_act);
   float* part = reinterpret_cast<float*>(base + off_part);
-  unsigned* tickets = reinterpret_cast<unsigned*>(base + off_tickets);
   cudaStream_t cs = as_stream(stream);
-  // the fragment pass also zeroes the slice counters and the status word that follows them:
-  // the array keeps the previous call's contents, and these must start at zero
-  W4A8_CUDA_TRY(act_prep_run(a_q, M, K, K, act, tickets, p.n_rg + 1, cs));
-  W4A8_CUDA_TRY(mm_run(p, w_t, s_t, act, a_s, M, y, N, EPI_STORE, part, tickets, tickets + p.n_rg, nullptr, cs));
+  // the fragment pass also zeroes the status word and the slice counters that follow it: the
+  // array keeps the previous call's contents, and these must start at zero
+  W4A8_CUDA_TRY(act_prep_run(a_q, M, K, K, act, status, p.n_rg + 1, cs));
+  W4A8_CUDA_TRY(mm_run(p, w_t, s_t, act, a_s, M, y, N, EPI_STORE, part, status + 1, status, nullptr, cs));
   return W4A8_OK;
+}
+
+W4A8_API w4a8_status w4a8_matmul_noalloc_check(uint32_t* flags) {
+  if (!flags) return W4A8_ERR_ARG;
+  void* base = nullptr;
+  const w4a8_status st = scratch_address(&base);
+  if (st != W4A8_OK) return st;
+  W4A8_CUDA_TRY(cudaMemcpy(flags, base, 4, cudaMemcpyDeviceToHost));
+  return *flags ? W4A8_ERR_DEVICE_FLAG : W4A8_OK;
 }
