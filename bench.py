@@ -3,7 +3,7 @@
 int4-g32 / int8-activation decoder on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload llama3-8b-ctx4096|qwen05b-ctx512|tiny]
+                    [--workload llama3-8b-ctx4096|qwen05b-ctx512|tiny] [--no-extras]
 
 One step = one generation of `max_new` tokens (256) from a prefilled 4096-token
 motif-repeated context: W-step CUDA-graph windows, two in flight, the device-timed width
@@ -16,14 +16,20 @@ end-to-end call (w4a8_decode: prompt copied from pinned host memory, prefill, wi
 tokens read back) on the host clock.  For N > 1 (torchrun) every rank runs an independent
 replica (the method is a single sequence: replicas only) and rank 0 reports the aggregate.
 
-`--impl reference` times the CPU oracle (the test oracle under oracle/) on a bounded sample
-of the same workload and prints the same JSON line with "impl": "reference".
+Extra keys of the same line (rank 0; skipped with --no-extras): the standalone W4A8 matmul
+sweep over the token counts and shapes of the matmul workload, the Qwen2.5-0.5B-shaped
+workload (verification step cost per width, the window-size sweep, decode modes), and the
+window test on the 8B-shaped model (a 2048-token prompt, W in {1, 4, 16}, host syncs).
+
+`--impl reference` times the CPU oracle (the test oracle under oracle/) on bounded samples
+and prints the same JSON line with "impl": "reference".
 """
 from __future__ import annotations
 
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -35,6 +41,7 @@ sys.path.insert(0, ROOT)
 
 MAX_NEW = 256
 WIDTHS = [1, 4, 8, 16]
+METRIC = "accepted tokens/s (GPU-resident tree-speculative greedy decoding)"
 
 WORKLOADS = {
     # name: (shape name, prompt tokens, motifs, motif length, substitution prob, seed)
@@ -42,6 +49,10 @@ WORKLOADS = {
     "qwen05b-ctx512": ("qwen2.5-0.5b-shaped", 512, 4, 16, 0.10, 1003),
     "tiny": ("tiny-2L-256h", 64, 4, 16, 0.10, 1001),
 }
+# the window test: 8B-shaped model, 2048 tokens of 8 motifs of 32 tokens, 30% substitutions
+WINDOW_TEST = ("llama3-8b-shaped", 2048, 8, 32, 0.30, 1005)
+MATMUL_SHAPES = [(896, 4864), (4864, 896), (4096, 14336), (14336, 4096), (4096, 128256)]
+MATMUL_TOKENS = [1, 2, 4, 8, 16]
 
 
 def parse():
@@ -52,10 +63,12 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama3-8b-ctx4096", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the extra workloads of the line")
     ap.add_argument("--new-tokens", type=int, default=MAX_NEW,
                     help="tokens generated per step (the workload's figure is %d)" % MAX_NEW)
     ap.add_argument("--matmul", type=int, nargs=3, metavar=("K", "N", "M"),
                     help="time one W4A8 matmul shape through the C ABI instead of the decoding step")
+    ap.add_argument("--oracle-worker", choices=["tiny", "sample"], help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -159,12 +172,18 @@ def mm_traffic(kernel_src):
     return None
 
 
-def run_matmul(args):
-    """One W4A8 matmul shape (K, N, M) through the C ABI: fragment pass + matmul per call,
-    weights rotated over copies larger than L2, CUDA events on the launching stream."""
+def matmul_bytes(K, N, M):
+    """Algorithmic bytes of one W4A8 product: packed weights, fp16 scales, int8 activations
+    and their scales, fp32 outputs."""
+    return N * K // 2 + N * (K // 32) * 2 + M * K + 4 * M + 4 * M * N
+
+
+def time_matmul(K, N, M, reps_min=20, trials=5):
+    """Device time of one standalone w4a8_matmul call (activation pass + matmul): a CUDA graph
+    of back-to-back calls, weights rotated over copies larger than L2, CUDA events on the
+    launching stream, median of the trials."""
     import torch
     import w4a8_verify_gb300 as W
-    K, N, M = args.matmul
     dev = torch.device("cuda")
     wb, sb = W.w4a8_weight_layout_bytes(N, K)
     copies = max(2, -(-(4 * 135 * 2**20) // (wb + sb)))
@@ -176,28 +195,88 @@ def run_matmul(args):
     a_q, a_s = W.w4a8_quantize_rows(x, 0)
     ws = torch.zeros(W.w4a8_matmul_workspace_bytes(M, K, N), dtype=torch.uint8, device=dev)
     y = torch.empty(M, N, device=dev)
-    stream = torch.cuda.current_stream()
-    for i in range(max(3, args.warmup)):
-        W.w4a8_matmul(a_q, a_s, wt[i % copies], st[i % copies], N, y=y, workspace=ws)
-    reps = max(args.steps, copies)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s = torch.cuda.Stream()
+    reps = max(reps_min, copies)
+    times = []
+    with torch.cuda.stream(s):
+        for i in range(3):
+            W.w4a8_matmul(a_q, a_s, wt[i % copies], st[i % copies], N, y=y, workspace=ws)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            for i in range(reps):
+                W.w4a8_matmul(a_q, a_s, wt[i % copies], st[i % copies], N, y=y, workspace=ws)
+        graph.replay()
+        for _ in range(trials):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            graph.replay()
+            e1.record(s)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3 / reps)
     torch.cuda.synchronize()
-    e0.record(stream)
-    for i in range(reps):
-        W.w4a8_matmul(a_q, a_s, wt[i % copies], st[i % copies], N, y=y, workspace=ws)
-    e1.record(stream)
-    e1.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / reps
-    alg = N * K // 2 + N * (K // 32) * 2 + M * K + 4 * M * N
-    return {"matmul": {"K": K, "N": N, "M": M}, "us_per_call": round(us, 3), "calls": reps,
-            "algorithmic_bytes": alg, "GBs": round(alg / us / 1e3, 1), "slices": W.w4a8_matmul_slices(K, N),
-            "includes": "activation fragment pass + matmul (2 kernels)"}
+    flags = W.w4a8_matmul_check(ws, M, K, N)
+    del wt, st, graph
+    us = statistics.median(times)
+    alg = matmul_bytes(K, N, M)
+    return {"K": K, "N": N, "M": M, "us": round(us, 3), "GBs": round(alg / us / 1e3, 1),
+            "slices": W.w4a8_matmul_slices(K, N), "flags": flags}
+
+
+def run_matmul(args):
+    K, N, M = args.matmul
+    r = time_matmul(K, N, M, reps_min=max(20, args.steps))
+    r["includes"] = "activation fragment pass + matmul (2 kernels) per call"
+    return r
+
+
+def timed_generate(sess, prompt_dev, max_new, stream, **kw):
+    """Prefill (untimed), then one generation timed with CUDA events on the launching stream:
+    (tokens/s, tokens, report)."""
+    import torch
+    sess.prefill(prompt_dev, max_new)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    toks, rep = sess.generate(max_new, **kw)
+    ev1.record(stream)
+    ev1.synchronize()
+    return len(toks) / (ev0.elapsed_time(ev1) / 1e3), toks, rep
+
+
+def window_sweep(sess, prompt_dev, stream, widths, t_us, windows, max_new=64, reps=3):
+    """Decode time per window size W (median of reps), and the smallest W within 10% of the
+    fastest (Feedback Control: the window size is chosen at load time)."""
+    res = {}
+    for Wn in windows:
+        ts = []
+        for _ in range(reps):
+            v, toks, rep = timed_generate(sess, prompt_dev, max_new, stream, window=Wn, widths=widths, t_us=t_us)
+            ts.append(1e3 * len(toks) / v)
+        res[Wn] = statistics.median(ts) / max_new
+    fastest = min(res.values())
+    chosen = min(w for w, t in res.items() if t <= 1.10 * fastest)
+    return chosen, {str(w): round(t, 4) for w, t in res.items()}
+
+
+def decode_modes(sess, prompt_dev, stream, max_new, widths, t_us, window):
+    """The decode modes of the pages' comparison on one prompt: greedy with a host read-back
+    after every token, the GPU loop at width 1 in windows, and speculation with the controller."""
+    out = {}
+    for name, kw in (("greedy_host_sync_per_token", dict(window=1, fixed_width=1, in_flight=1)),
+                     ("gpu_loop_width1_window8", dict(window=8, fixed_width=1, in_flight=2)),
+                     ("spec_controller", dict(window=window, widths=widths, t_us=t_us))):
+        try:
+            v, toks, rep = timed_generate(sess, prompt_dev, max_new, stream, **kw)
+            out[name] = {"tokens_per_s": round(v, 2), "steps": rep.n_steps, "host_syncs": rep.host_syncs,
+                         "tau": round(len(toks) / max(1, rep.n_steps), 3)}
+        except Exception as exc:  # reported, never fatal to the line
+            out[name] = "failed: %s" % exc
+    return out
 
 
 # --------------------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world):
-    import numpy as np
     import torch
     import synth
     import w4a8_verify_gb300 as W
@@ -221,15 +300,7 @@ def run_ours(args, rank, world):
     # load-time calibration [Feedback Control]: T(N) per width, then the window size
     sess.prefill(prompt_dev, MAX_NEW)
     t_us = sess.calibrate(WIDTHS, reps=10, trials=5)
-    win_t = {}
-    for Wn in (1, 2, 4):
-        sess.prefill(prompt_dev, 64)
-        torch.cuda.synchronize()
-        a = time.perf_counter()
-        sess.generate(64, window=Wn, widths=WIDTHS, t_us=t_us)
-        win_t[Wn] = time.perf_counter() - a
-    fastest = min(win_t.values())
-    window = min(w for w, t in win_t.items() if t <= 1.10 * fastest)
+    window, _ = window_sweep(sess, prompt_dev, stream, WIDTHS, t_us, (1, 2, 4), reps=1)
 
     def one_step(timed=False):
         sess.prefill(prompt_dev, MAX_NEW)
@@ -278,6 +349,13 @@ def run_ours(args, rank, world):
             e2e_ms.append((b - a) * 1e3)
     e2e_value = MAX_NEW / (statistics.median(e2e_ms) / 1e3)
     d2h = rep_e.n_windows * (32 + window * (12 + 64))
+    # time to first token through the public call (prompt upload + prefill + one step + read-back)
+    ttft = []
+    for _ in range(3):
+        torch.cuda.synchronize()
+        a = time.perf_counter()
+        sess.decode(prompt_list, 1, window=1, fixed_width=1, in_flight=1)
+        ttft.append((time.perf_counter() - a) * 1e3)
 
     # dominant kernel: the W4A8 matmul launches of one verification pass (events over a graph)
     sess.prefill(prompt_dev, MAX_NEW)
@@ -299,32 +377,14 @@ def run_ours(args, rank, world):
     achieved = bytes1 / us1 / 1e3
     trf = mm_traffic(os.path.join(ROOT, "w4a8_verify_gb300", "csrc", "matmul.cu"))
 
-    # decode modes of the pages' comparison on the same prompt and token count (not part of
-    # `value`): greedy with a host read-back after every token, the GPU loop at width 1 in
-    # windows of 8, and the speculation loop with the controller (= value)
-    modes = {}
-    for name, kw in (("greedy_host_sync_per_token", dict(window=1, fixed_width=1, in_flight=1)),
-                     ("gpu_loop_width1_window8", dict(window=8, fixed_width=1, in_flight=2))):
-        try:
-            sess.prefill(prompt_dev, MAX_NEW)
-            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            ev0.record(stream)
-            toks_m, _ = sess.generate(MAX_NEW, **kw)
-            ev1.record(stream)
-            ev1.synchronize()
-            modes[name] = round(len(toks_m) / (ev0.elapsed_time(ev1) / 1e3), 2)
-        except Exception as exc:  # reported, never fatal to the line
-            modes[name] = "failed: %s" % exc
-    modes["spec_controller"] = round(value, 2)
+    modes = decode_modes(sess, prompt_dev, stream, MAX_NEW, WIDTHS, t_us, window)
 
     launches = sum(int(r.kernels) for r in reps)  # kernel nodes of the window graphs run while timed
-    mean_rep = reps[-1]
     steps_total = sum(r.n_steps for r in reps)
     wsteps = {w: sum(r.width_steps[w] for r in reps) for w in WIDTHS}
     clocks = clk.summary()
     line = {
-        "metric": "accepted tokens/s (GPU-resident tree-speculative greedy decoding)",
+        "metric": METRIC,
         "value": round(value, 2),
         "unit": "tokens/s",
         "n_gpus": world,
@@ -348,43 +408,149 @@ def run_ours(args, rank, world):
             "l2": "weights 4.2 GB >> L2 (inputs larger than L2)",
         },
         "e2e": {"value": round(e2e_value, 2), "unit": "tokens/s", "h2d_bytes_per_step": plen * 4,
-                "d2h_bytes_per_step": d2h, "includes": "prompt upload + prefill + decode + token read-back"},
+                "d2h_bytes_per_step": d2h, "includes": "prompt upload + prefill + decode + token read-back",
+                "ttft_ms": round(statistics.median(ttft), 2)},
         "gpu_launches": launches,
         "clocks": clocks,
         "roofline": {
             "bound": "hbm", "kernel": "k_mm (W4A8 matmul, N=1 verification pass)",
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "peak_source": "MEASURED_PEAKS.json hbm_gbs" if peaks else "fallback",
+            "frac": round(achieved / peak, 4),
+            "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks else "fallback",
             "traffic": trf,
             "algorithmic_bytes_per_launch": round(bytes1),
             "us_per_launch": round(us1, 3), "launches_per_pass": nl,
-            "by_width": {str(N): {"us_per_launch": round(v[0], 3), "GBs": round(v[1] / v[0] / 1e3, 1)}
+            "by_width": {str(N): {"us_per_launch": round(v[0], 3), "GBs": round(v[1] / v[0] / 1e3, 1),
+                                  "frac": round(v[1] / v[0] / 1e3 / peak, 4)}
                          for N, v in mm.items()},
         },
         "verify_step_us": {str(w): round(t, 1) for w, t in zip(WIDTHS, t_us)},
-        "decode_modes_tokens_per_s": modes,
         "verify_ratio_8_over_1": round(t_us[2] / t_us[0], 3),
+        "decode_modes": modes,
         "tau_tokens_per_step": round(MAX_NEW * args.steps / max(1, steps_total), 3),
         "width_steps": wsteps,
         "host_syncs_per_step": round(sum(r.host_syncs for r in reps) / args.steps, 1),
         "setup_s": round(t_build, 1),
     }
+    if rank == 0 and world == 1 and not args.no_extras and args.workload == "llama3-8b-ctx4096":
+        line["extras"] = run_extras(model, torch, stream)
     return line
 
 
-# --------------------------------------------------------------------------- oracle arm
+def run_extras(model8b, torch, stream):
+    """The other workloads, each reported beside the headline (not part of `value`)."""
+    import synth
+    import w4a8_verify_gb300 as W
+    out = {}
+    dev = torch.device("cuda")
+    # matmul workload: every token count and shape, standalone calls through the C ABI
+    sweep = []
+    for K, N in MATMUL_SHAPES:
+        for M in MATMUL_TOKENS:
+            try:
+                sweep.append(time_matmul(K, N, M))
+            except Exception as exc:
+                sweep.append({"K": K, "N": N, "M": M, "failed": str(exc)})
+    out["matmul_sweep"] = {"unit": "us per call, GB/s algorithmic", "calls": sweep,
+                           "includes": "activation fragment pass + matmul (2 kernels) per call"}
 
-def oracle_sample(args, steps, warmup):
-    """Times the CPU oracle on a bounded sample of the workload: one decoding step of
-    one decoder layer of the workload's shape (attention over the full prompt-length
-    context) plus 1/32 of the LM head rows; the per-token time is scaled to all layers and
-    the full head.  Weights are uniform int4 codes with fp16 scales from the seeded
-    generator (the oracle's cost does not depend on the values)."""
+    # Qwen2.5-0.5B-shaped workload: 512-token prompt, 256 tokens, widths {1,2,4,8,16}
+    sh_name, plen, nmot, mlen, psub, seed = WORKLOADS["qwen05b-ctx512"]
+    shape = synth.SHAPES[sh_name]
+    m = build_model(shape, seed)
+    prompt = synth.motif_prompt(seed, plen, nmot, mlen, psub, shape.vocab)
+    pd = torch.from_numpy(prompt).to(dev)
+    s = W.Session(m, plen + MAX_NEW + 64, plen + MAX_NEW + 96, max_window=16)
+    widths = [1, 2, 4, 8, 16]
+    s.prefill(pd, MAX_NEW)
+    t_us = s.calibrate(widths, reps=20, trials=5)
+    chosen, per_tok = window_sweep(s, pd, stream, widths, t_us, (1, 2, 4, 8, 16), max_new=128, reps=3)
+    modes = decode_modes(s, pd, stream, MAX_NEW, widths, t_us, chosen)
+    s.prefill(pd, MAX_NEW)
+    us1, by1, nl = s.time_matmuls(1, reps=50)
+    out["qwen05b-ctx512"] = {
+        "model": sh_name, "prompt_tokens": plen, "new_tokens": MAX_NEW,
+        "verify_step_us": {str(w): round(t, 1) for w, t in zip(widths, t_us)},
+        "verify_ratio_over_1": {str(w): round(t / t_us[0], 3) for w, t in zip(widths, t_us)},
+        "window_sweep_ms_per_token": per_tok, "window_chosen": chosen,
+        "decode_modes": modes,
+        "matmul_pass": {"us_per_launch": round(us1, 3), "GBs": round(by1 / us1 / 1e3, 1), "launches": nl},
+    }
+    s.close()
+    del s, m
+    torch.cuda.empty_cache()
+
+    # window test on the 8B-shaped model: 2048 tokens of 32-token motifs, 30% substitutions
+    sh_name, plen, nmot, mlen, psub, seed = WINDOW_TEST
+    prompt = synth.motif_prompt(seed, plen, nmot, mlen, psub, synth.SHAPES[sh_name].vocab)
+    pd = torch.from_numpy(prompt).to(dev)
+    new = 512
+    s = W.Session(model8b, plen + new + 64, plen + new + 96, max_window=16)
+    s.prefill(pd, new)
+    t_us = s.calibrate(WIDTHS, reps=10, trials=3)
+    runs = {}
+    for Wn in (1, 4, 16):
+        v, toks, rep = timed_generate(s, pd, new, stream, window=Wn, widths=WIDTHS, t_us=t_us)
+        runs[str(Wn)] = {"tokens_per_s": round(v, 2), "steps": rep.n_steps, "windows": rep.n_windows,
+                         "host_syncs": rep.host_syncs, "tau": round(len(toks) / max(1, rep.n_steps), 3),
+                         "accepted_drafts_per_step": round(rep.accepted_drafts / max(1, rep.n_steps), 3),
+                         "width_steps": {str(w): rep.width_steps[w] for w in WIDTHS}}
+    out["window_test"] = {"model": sh_name, "prompt": "%d tokens, %d motifs x %d, substitution p=%.2f" %
+                          (plen, nmot, mlen, psub), "new_tokens": new, "by_window": runs}
+    s.close()
+    return out
+
+
+# --------------------------------------------------------------------------- oracle timing
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True,
+                             timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return "%s (%s)" % (ln.split(":", 1)[1].strip(), platform.machine())
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu model")):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def oracle_tiny():
+    """The oracle decoding the tiny workload for real: 32 greedy tokens, then 32 speculative
+    tokens at width 8, from the 64-token motif prompt."""
+    import synth
+    from oracle import model as OM
+    from oracle import spec as OS
+    sh_name, plen, nmot, mlen, psub, seed = WORKLOADS["tiny"]
+    ow = OM.build_weights(synth.SHAPES[sh_name], 1000)
+    prompt = synth.motif_prompt(seed, plen, nmot, mlen, psub, synth.SHAPES[sh_name].vocab)
+    a = time.perf_counter()
+    g, _ = OM.greedy_decode(ow, prompt, 32)
+    b = time.perf_counter()
+    s, st = OS.spec_decode(ow, prompt, 32, 8)
+    c = time.perf_counter()
+    assert s == g
+    return {"greedy_tokens_per_s": round(32 / (b - a), 3), "spec_tokens_per_s": round(32 / (c - b), 3),
+            "spec_steps": len(st), "greedy_s": round(b - a, 3), "spec_s": round(c - b, 3)}
+
+
+def oracle_sample(workload, steps, warmup):
+    """Times the CPU oracle on a bounded sample of the workload: one decoding step of one
+    decoder layer of the workload's shape (attention over the full prompt-length context)
+    plus 1/32 of the LM head rows.  Weights are uniform int4 codes with fp16 scales from the
+    seeded generator (the oracle's cost does not depend on the values).  Returns the
+    measured sample times and the per-token time scaled to all layers and the full head."""
     import numpy as np
     import synth
     from oracle import model as OM
 
-    shape_name, plen, *_ = WORKLOADS[args.workload]
+    shape_name, plen, *_ = WORKLOADS[workload]
     sh = synth.SHAPES[shape_name]
     one = synth.ModelShape(sh.name + "-1layer", 1, sh.hidden, sh.n_heads, sh.n_kv_heads, sh.head_dim, sh.ffn,
                            sh.ffn_real, sh.vocab // 32 // 16 * 16, False)
@@ -404,49 +570,79 @@ def oracle_sample(args, steps, warmup):
     kv = synth.normal(7, 50, 0, sh.n_kv_heads * plen * sh.head_dim, 1.0).reshape(sh.n_kv_heads, plen, sh.head_dim)
     m.K[0][:, :plen] = kv
     m.V[0][:, :plen] = kv[:, ::-1]
-    cores = len(os.sched_getaffinity(0))
-    # warm the dequantised-weight cache (not timed)
-    m.step(3, plen)
-    per_token = []
+    m.step(3, plen)  # warm the dequantised-weight cache (not timed)
+    samples = []
     for i in range(warmup + steps):
         a = time.perf_counter()
-        tr = {}
-        m.forward([3], [plen], [plen], [list(range(plen + 1))], trace=tr)
-        t_layer_and_head = time.perf_counter() - a
+        m.forward([3], [plen], [plen], [list(range(plen + 1))])
         if i >= warmup:
-            per_token.append(t_layer_and_head)
-    # split: time of the 1/32 head alone, to scale layer and head separately
-    import numpy as _np
-    x = _np.random.default_rng(0).normal(size=sh.hidden)
+            samples.append(time.perf_counter() - a)
+    x = np.random.default_rng(0).normal(size=sh.hidden)
     a = time.perf_counter()
     m.linear("lm", w.lm_head, x)
     t_head = time.perf_counter() - a
-    t_layer = statistics.median(per_token) - t_head
+    t_layer = statistics.median(samples) - t_head
     t_tok = sh.n_layers * t_layer + t_head * (sh.vocab / one.vocab)
-    return 1.0 / t_tok, cores, per_token, t_tok
+    return samples, t_tok
 
 
-def cpu_baseline_line(args):
-    v, cores, samples, t_tok = oracle_sample(args, steps=2, warmup=1)
-    return {"value": round(v, 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": "one plain greedy step of one decoder layer (full-context attention) + 1/32 of the LM head, "
-                      "scaled to all layers and the full head; %.1f s per token" % t_tok}
+def oracle_worker(kind, workload, steps, warmup):
+    """Runs in a child process whose BLAS thread count is set by its environment."""
+    if kind == "tiny":
+        r = oracle_tiny()
+    else:
+        samples, t_tok = oracle_sample(workload, steps, warmup)
+        r = {"samples_s": [round(x, 4) for x in samples], "t_token_s": t_tok}
+    print(json.dumps(r), flush=True)
+
+
+def run_oracle_child(kind, threads, workload="llama3-8b-ctx4096", steps=2, warmup=1, timeout=600):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = str(threads)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-worker", kind, "--workload", workload,
+           "--steps", str(steps), "--warmup", str(warmup)]
+    r = subprocess.run(cmd, env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, timeout=timeout)
+    if r.returncode != 0:
+        raise RuntimeError("oracle worker failed: %s" % r.stderr[-400:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline_line(workload):
+    cores = len(os.sched_getaffinity(0))
+    smp = run_oracle_child("sample", cores, workload, steps=2, warmup=1)
+    tiny1 = run_oracle_child("tiny", 1)
+    tinyn = run_oracle_child("tiny", cores)
+    return {"value": round(1.0 / smp["t_token_s"], 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "cpu": cpu_model(),
+            "sample": "timed: %d decoding steps of one full-size decoder layer (attention over the whole "
+                      "context) plus 1/32 of the LM head rows (%s s each); value = 1 / (per-token time scaled "
+                      "to all layers and the full head)" % (len(smp["samples_s"]), smp["samples_s"]),
+            "tiny_decode": {"workload": "tiny (2 layers, hidden 256, 64-token prompt, 32 new tokens)",
+                            "threads_1": tiny1, "threads_%d" % cores: tinyn}}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    v, cores, samples, t_tok = oracle_sample(args, steps=args.steps, warmup=args.warmup)
+    cores = len(os.sched_getaffinity(0))
+    t0 = time.perf_counter()
+    smp = run_oracle_child("sample", cores, args.workload, steps=args.steps, warmup=args.warmup,
+                           timeout=3000)
+    wall = time.perf_counter() - t0
+    v = 1.0 / smp["t_token_s"]
     shape_name = WORKLOADS[args.workload][0]
+    samples = smp["samples_s"]
     return {
         "impl": "reference",
-        "metric": "accepted tokens/s (GPU-resident tree-speculative greedy decoding)",
+        "metric": METRIC,
         "value": round(v, 5),
         "unit": "tokens/s",
         "n_gpus": world,
-        "steps": args.steps,
+        "steps": len(samples),
         "warmup": args.warmup,
-        "ms_per_step": round(t_tok * 1e3, 1),
+        "ms_per_step": round(1e3 * statistics.mean(samples), 1),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -454,17 +650,31 @@ def run_reference(args, rank, world):
         "data": "synthetic",
         "config": {"workload": args.workload, "model": shape_name, "prompt_tokens": WORKLOADS[args.workload][1],
                    "new_tokens_per_step": MAX_NEW, "widths": WIDTHS,
-                   "parallelism": "replicas" if world > 1 else "single"},
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "timed_unit": "one sample = one decoding step of one full-size decoder layer (attention over "
+                                 "the whole context) + 1/32 of the LM head rows; ms_per_step is per sample",
+                   "scaled": "value = 1 / (%d x layer time + 32 x the 1/32-head time) = %.1f s per token"
+                             % (synth_layers(shape_name), smp["t_token_s"]),
+                   "wall_s": round(wall, 1)},
         "cpu_baseline": {"value": round(v, 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": "one plain greedy step of one decoder layer + 1/32 LM head per step, scaled"},
+                         "cpu": cpu_model(),
+                         "sample": "%d samples of one layer + 1/32 LM head, scaled to the full model" % len(samples)},
         "e2e": {"value": round(v, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+def synth_layers(shape_name):
+    import synth
+    return synth.SHAPES[shape_name].n_layers
 
 
 def main():
     global MAX_NEW
     args = parse()
     MAX_NEW = args.new_tokens
+    if args.oracle_worker:
+        oracle_worker(args.oracle_worker, args.workload, args.steps, args.warmup)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
     if args.impl == "reference":
@@ -488,7 +698,7 @@ def main():
     line = run_ours(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline_line(args)
+            line["cpu_baseline"] = cpu_baseline_line(args.workload)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
