@@ -68,6 +68,8 @@ def parse():
                     help="tokens generated per step (the workload's figure is %d)" % MAX_NEW)
     ap.add_argument("--matmul", type=int, nargs=3, metavar=("K", "N", "M"),
                     help="time one W4A8 matmul shape through the C ABI instead of the decoding step")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="decoder layers of the model (0 = the workload's; fewer only for small profiling runs)")
     ap.add_argument("--oracle-worker", choices=["tiny", "sample"], help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -178,13 +180,15 @@ def matmul_bytes(K, N, M):
     return N * K // 2 + N * (K // 32) * 2 + M * K + 4 * M + 4 * M * N
 
 
-def time_matmul(K, N, M, reps_min=20, trials=5):
-    """Device time of one standalone w4a8_matmul call (activation pass + matmul): a CUDA graph
-    of back-to-back calls, weights rotated over copies larger than L2, CUDA events on the
-    launching stream, median of the trials."""
+def time_matmul(K, N, M, reps_min=20, trials=5, variant="det"):
+    """Device time of one standalone matmul call (activation pass + matmul): a CUDA graph of
+    back-to-back calls, weights rotated over copies larger than L2, CUDA events on the launching
+    stream, median of the trials.  variant: "det" (w4a8_matmul), "nondet" (w4a8_matmul_nondet,
+    slices added with atomics), "per32" (w4a8_matmul_per32, one activation scale per 32 inputs)."""
     import torch
     import w4a8_verify_gb300 as W
     dev = torch.device("cuda")
+    call = {"det": W.w4a8_matmul, "nondet": W.w4a8_matmul_nondet, "per32": W.w4a8_matmul_per32}[variant]
     wb, sb = W.w4a8_weight_layout_bytes(N, K)
     copies = max(2, -(-(4 * 135 * 2**20) // (wb + sb)))
     g = torch.Generator(device=dev).manual_seed(7)
@@ -192,7 +196,7 @@ def time_matmul(K, N, M, reps_min=20, trials=5):
           for _ in range(copies)]
     st = [torch.full((sb // 2,), 0x2000, dtype=torch.int16, device=dev) for _ in range(copies)]
     x = torch.randn(M, K, device=dev, generator=g)
-    a_q, a_s = W.w4a8_quantize_rows(x, 0)
+    a_q, a_s = W.w4a8_quantize_rows(x, 1 if variant == "per32" else 0)
     ws = torch.zeros(W.w4a8_matmul_workspace_bytes(M, K, N), dtype=torch.uint8, device=dev)
     y = torch.empty(M, N, device=dev)
     s = torch.cuda.Stream()
@@ -200,11 +204,11 @@ def time_matmul(K, N, M, reps_min=20, trials=5):
     times = []
     with torch.cuda.stream(s):
         for i in range(3):
-            W.w4a8_matmul(a_q, a_s, wt[i % copies], st[i % copies], N, y=y, workspace=ws)
+            call(a_q, a_s, wt[i % copies], st[i % copies], N, y=y, workspace=ws)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=s):
             for i in range(reps):
-                W.w4a8_matmul(a_q, a_s, wt[i % copies], st[i % copies], N, y=y, workspace=ws)
+                call(a_q, a_s, wt[i % copies], st[i % copies], N, y=y, workspace=ws)
         graph.replay()
         for _ in range(trials):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -285,6 +289,10 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda")
     shape_name, plen, nmot, mlen, psub, seed = WORKLOADS[args.workload]
     shape = synth.SHAPES[shape_name]
+    if args.layers > 0:
+        import dataclasses
+        shape = dataclasses.replace(shape, name="%s-%dlayer" % (shape.name, args.layers), n_layers=args.layers)
+        shape_name = shape.name
     t0 = time.time()
     model = build_model(shape, seed)
     torch.cuda.synchronize()
@@ -349,6 +357,16 @@ def run_ours(args, rank, world):
             e2e_ms.append((b - a) * 1e3)
     e2e_value = MAX_NEW / (statistics.median(e2e_ms) / 1e3)
     d2h = rep_e.n_windows * (32 + window * (12 + 64))
+    # one prefill on its own (device events; an NVTX range lets a profiler select its launches)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("prefill")
+    ev0.record(stream)
+    sess.prefill(prompt_dev, MAX_NEW)
+    ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.nvtx.range_pop()
+    prefill_ms = ev0.elapsed_time(ev1)
     # time to first token through the public call (prompt upload + prefill + one step + read-back)
     ttft = []
     for _ in range(3):
@@ -405,11 +423,13 @@ def run_ours(args, rank, world):
             "window": window,
             "windows_in_flight": 2,
             "parallelism": "replicas" if world > 1 else "single",
-            "l2": "weights 4.2 GB >> L2 (inputs larger than L2)",
+            "l2": "weights %.2f GB %s L2 (129 MB)" % (model.weight_bytes() / 1e9,
+                                                      ">>" if model.weight_bytes() > 4 * 129e6 else "vs"),
         },
         "e2e": {"value": round(e2e_value, 2), "unit": "tokens/s", "h2d_bytes_per_step": plen * 4,
                 "d2h_bytes_per_step": d2h, "includes": "prompt upload + prefill + decode + token read-back",
-                "ttft_ms": round(statistics.median(ttft), 2)},
+                "ttft_ms": round(statistics.median(ttft), 2),
+                "prefill_ms": round(prefill_ms, 2), "prefill_tokens_per_s": round((plen - 1) / (prefill_ms / 1e3), 1)},
         "gpu_launches": launches,
         "clocks": clocks,
         "roofline": {
@@ -432,7 +452,7 @@ def run_ours(args, rank, world):
         "host_syncs_per_step": round(sum(r.host_syncs for r in reps) / args.steps, 1),
         "setup_s": round(t_build, 1),
     }
-    if rank == 0 and world == 1 and not args.no_extras and args.workload == "llama3-8b-ctx4096":
+    if rank == 0 and world == 1 and not args.no_extras and args.workload == "llama3-8b-ctx4096" and not args.layers:
         line["extras"] = run_extras(model, torch, stream)
     return line
 
@@ -453,6 +473,22 @@ def run_extras(model8b, torch, stream):
                 sweep.append({"K": K, "N": N, "M": M, "failed": str(exc)})
     out["matmul_sweep"] = {"unit": "us per call, GB/s algorithmic", "calls": sweep,
                            "includes": "activation fragment pass + matmul (2 kernels) per call"}
+    # cost of exactness: the fixed-order (deterministic) product against the variant that adds the
+    # K slices with atomics, and the per-32 activation-scale form
+    cost = []
+    for K, N in MATMUL_SHAPES:
+        for M in (1, 16):
+            try:
+                r = {"K": K, "N": N, "M": M}
+                for v in ("det", "nondet", "per32"):
+                    r[v + "_us"] = time_matmul(K, N, M, variant=v)["us"]
+                r["det_over_nondet"] = round(r["det_us"] / r["nondet_us"], 3)
+                r["per32_over_det"] = round(r["per32_us"] / r["det_us"], 3)
+                cost.append(r)
+            except Exception as exc:
+                cost.append({"K": K, "N": N, "M": M, "failed": str(exc)})
+    out["exactness_cost"] = {"unit": "us per call", "rows": cost,
+                             "note": "nondet: slices combined with float atomics in arrival order"}
 
     # Qwen2.5-0.5B-shaped workload: 512-token prompt, 256 tokens, widths {1,2,4,8,16}
     sh_name, plen, nmot, mlen, psub, seed = WORKLOADS["qwen05b-ctx512"]

@@ -120,6 +120,27 @@ w4a8_status w4a8_matmul(const int8_t* a_q, const float* a_s, int M, int K, const
                         const uint16_t* s_t, int N, float* y, void* workspace, size_t workspace_bytes,
                         void* stream);
 
+/* Device.  w4a8_matmul with per-32 activation scales [P1 Small-Batch Verification Kernels:
+ * activations carry one scale per block of 32 values]: a_s is fp32 [M][K/32] (device; e.g. from
+ * w4a8_quantize_rows mode 1), and
+ *   y[t][n] = sum_g (s_w[n][g] * s_a[t][g]) * isum[t][n][g]
+ * in the fixed order of w4a8_matmul with acc = fmaf(s_w * s_a[t][g] (rounded once), isum, acc)
+ * per group and no final multiply.  Same limits and workspace as w4a8_matmul. */
+w4a8_status w4a8_matmul_per32(const int8_t* a_q, const float* a_s, int M, int K, const uint32_t* w_t,
+                              const uint16_t* s_t, int N, float* y, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/* Device.  The fast, non-deterministic variant of w4a8_matmul [P1 Implementation: the
+ * deterministic mode fixes the reduction order at a cost the paper measures as 0-15%]: the same
+ * exact integer group sums and per-slice fmaf chains, but the K slices of each output are added
+ * into y (zeroed by this call) with float atomics in arrival order instead of the fixed left fold,
+ * so the last bits of y may vary between calls and M tokens need not give the bits of M single
+ * calls.  Same arguments, limits and workspace as w4a8_matmul (the workspace status word reports
+ * an expired wait; the split-K partial area is not used). */
+w4a8_status w4a8_matmul_nondet(const int8_t* a_q, const float* a_s, int M, int K, const uint32_t* w_t,
+                               const uint16_t* s_t, int N, float* y, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
 /* Host, synchronous.  Reads the device status word of a matmul workspace (call after the
  * stream has finished).  *flags = 0 if every bounded pipeline wait of the kernels that
  * used this workspace completed; otherwise it holds W4A8_FLAG_ERR_TIMEOUT (16) and the call
@@ -207,6 +228,7 @@ typedef struct {
   int ctx_cap;      /* context token capacity (>= prompt + max_new + 9) */
   int max_window;   /* largest window W of spec_window (1..64) */
   int eos_id;       /* stop token, or -1 */
+  int mem_cap;      /* session-memory entries (0..32768; ctx_cap + mem_cap <= 225280), 0 = none */
 } w4a8_session_desc;
 
 /* The 32-byte device control state [P1 GPU-Resident Speculation Loop]. */
@@ -359,6 +381,20 @@ w4a8_status w4a8_session_get_tree(w4a8_session* s, int32_t* tok, int32_t* parent
 w4a8_status w4a8_session_get_pred(w4a8_session* s, int32_t* pred, int n);
 /* Copies the context tokens (host int32[cap]); *n = context length. */
 w4a8_status w4a8_session_get_context(w4a8_session* s, int32_t* out, int cap, int* n);
+/* Session memory [P1 Draft-Free Drafting From Web Context: the drafter's scan also covers a
+ * buffer of the model's outputs from earlier requests; Experiments: a 32K-token budget].  The
+ * memory holds earlier outputs, each preceded by the separator -1, oldest first, in at most
+ * mem_cap entries (whole outputs are dropped from the oldest; an output longer than the memory
+ * keeps its last mem_cap - 1 tokens).  The drafter scans it as if it preceded the context: a
+ * match or a continuation never crosses a separator, and among equal match lengths a context
+ * position counts as more recent than any memory position.  It enters neither the KV cache nor
+ * the prefill.  Host, synchronous; not while windows are in flight (W4A8_ERR_ARG).
+ * append: tokens host int32[n] in [0, vocab); W4A8_ERR_CAPACITY if the session has mem_cap < 2.
+ * get: copies min(cap, entries) entries to out (host) and sets *n to the number of entries. */
+w4a8_status w4a8_session_memory_append(w4a8_session* s, const int32_t* tokens, int n);
+w4a8_status w4a8_session_memory_clear(w4a8_session* s);
+w4a8_status w4a8_session_memory_get(const w4a8_session* s, int32_t* out, int cap, int* n);
+
 /* Tree attention of one layer alone [P1 GPU-Resident Speculation Loop: each node attends to
  * the committed cache and to its ancestors], on the session's cache, committed length L and tree,
  * for caller-supplied queries: node i (0 <= i < n) attends to cache slots [0, L) and to the

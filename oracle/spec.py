@@ -132,22 +132,77 @@ def match_lengths(ctx, max_order: int = MAX_ORDER) -> np.ndarray:
     return out
 
 
-def draft(ctx, N: int, n_cand: int = N_CAND, max_cont: int = MAX_CONT):
-    """Next tree of N nodes from context ``ctx`` (whose last token is the root).
+SEP = -1  # separates the earlier outputs held in a session memory (equal to no token)
+
+
+def memory_array(segments, cap: int = 1 << 15):
+    """The session memory of Design > Draft-Free Drafting From Web Context (the drafter's scan
+    also covers a buffer of the model's outputs from earlier requests), as one token array:
+    every earlier output preceded by SEP, oldest first, keeping at most ``cap`` entries (whole
+    outputs are dropped from the oldest; an output longer than the memory keeps its last
+    cap - 1 tokens)."""
+    mem = []
+    for seg in segments:
+        seg = [int(t) for t in seg]
+        if len(seg) + 1 > cap:
+            seg = seg[len(seg) - (cap - 1):]
+        while mem and len(mem) + len(seg) + 1 > cap:
+            nxt = mem.index(SEP, 1) if SEP in mem[1:] else len(mem)
+            mem = mem[nxt:]
+        mem += [SEP] + seg
+    return mem
+
+
+def match_lengths_with_memory(mem, ctx, max_order: int = MAX_ORDER) -> np.ndarray:
+    """l(v) over the scan positions v of the sequence mem + ctx (every memory position, then the
+    context positions but its last): the length of the run of tokens ending at v that equals the
+    context suffix, within the memory (a SEP ends it) or within the context."""
+    m = len(mem)
+    c = [int(t) for t in ctx]
+    n = len(c)
+    out = np.zeros(m + max(n - 1, 0), dtype=np.int32)
+    for v in range(m):
+        l = 0
+        while l < max_order and v - l >= 0 and l < n and mem[v - l] == c[n - 1 - l]:
+            l += 1
+        out[v] = l
+    out[m:] = match_lengths(c, max_order)
+    return out
+
+
+def draft(ctx, N: int, n_cand: int = N_CAND, max_cont: int = MAX_CONT, memory=()):
+    """Next tree of N nodes from context ``ctx`` (whose last token is the root) and an optional
+    session memory (``memory_array``), scanned as if it preceded the context: a memory match
+    continues with the tokens after it up to the next SEP, and among equal match lengths a
+    context position is more recent than any memory position.
 
     Returns (tok int32[N], parent int32[N] with parent[0] = -1, n_valid, best_match_len)."""
     c = [int(t) for t in ctx]
     n = len(c)
-    ell = match_lengths(c)
-    cand = sorted((p for p in range(n - 1) if ell[p] >= 1), key=lambda p: (-int(ell[p]), -p))[:n_cand]
+    mem = [int(t) for t in memory]
+    m = len(mem)
+    ell = match_lengths_with_memory(mem, c)
+    cand = sorted((v for v in range(len(ell)) if ell[v] >= 1), key=lambda v: (-int(ell[v]), -v))[:n_cand]
     best = int(ell[cand[0]]) if cand else 0
+
+    def continuation(v):
+        if v >= m:
+            p = v - m
+            return c[p + 1: min(p + max_cont, n - 1) + 1]
+        out = []
+        for t in mem[v + 1: v + 1 + max_cont]:
+            if t == SEP:
+                break
+            out.append(t)
+        return out
+
     # weighted trie; node 0 is the root token
     node_tok, node_par, node_dep, node_score = [c[-1]], [-1], [0], [0]
     children = {}
     for p in cand:
         w = int(ell[p])
         cur = 0
-        for t in c[p + 1: min(p + max_cont, n - 1) + 1]:
+        for t in continuation(p):
             key = (cur, t)
             if key not in children:
                 children[key] = len(node_tok)
@@ -181,8 +236,9 @@ def draft(ctx, N: int, n_cand: int = N_CAND, max_cont: int = MAX_CONT):
 
 
 def spec_decode(weights, prompt, max_new: int, widths, eos: int = -1, kv_cap: int | None = None,
-                record=None):
-    """Speculative greedy decoding.  ``widths`` is an int or a callable step -> N.
+                record=None, memory=()):
+    """Speculative greedy decoding.  ``widths`` is an int or a callable step -> N; ``memory`` a
+    session memory (``memory_array``) the drafter scans besides the context.
 
     Returns (tokens, stats) with stats = list of (n_accepted_drafts, best_match_len, n_valid)."""
     prompt = [int(t) for t in prompt]
@@ -198,7 +254,7 @@ def spec_decode(weights, prompt, max_new: int, widths, eos: int = -1, kv_cap: in
     step = 0
     while len(out) < max_new:
         N = int(wfun(step))
-        tok, parent, n_valid, best = draft(ctx, N)
+        tok, parent, n_valid, best = draft(ctx, N, memory=memory)
         logits = tree_verify(m, L_c, tok, parent)
         pred = [argmax_lowest(logits[i]) for i in range(N)]
         path, emitted = accept(tok, parent, pred, n_valid)

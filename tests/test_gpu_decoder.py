@@ -80,8 +80,8 @@ def tiny():
     print("\n[tiny decoder parity] " + TALLY.summary())
 
 
-def _session(t, kv_cap=256, ctx_cap=512, max_window=16, eos=-1):
-    return W.Session(t["model"], kv_cap, ctx_cap, max_window, eos)
+def _session(t, kv_cap=256, ctx_cap=512, max_window=16, eos=-1, mem_cap=0):
+    return W.Session(t["model"], kv_cap, ctx_cap, max_window, eos, mem_cap)
 
 
 def _dev(a, dtype=torch.int32):
@@ -280,6 +280,61 @@ def test_draft_matches_oracle_on_random_contexts(tiny, seed):
     o_tok, o_par, o_nv, o_best = OS.draft(ctx.tolist(), 16)
     assert (n_valid, best) == (o_nv, o_best)
     assert tok[:n_valid] == o_tok[:n_valid].tolist() and par[1:n_valid] == o_par[1:n_valid].tolist()
+
+
+# --------------------------------------------------------------------- session memory
+
+def test_memory_append_follows_the_oracle_rule(tiny):
+    rng = np.random.default_rng(90)
+    for cap in (2, 7, 40, 300):
+        s = _session(tiny, mem_cap=cap)
+        segs = []
+        for _ in range(6):
+            seg = rng.integers(0, SHAPE.vocab, size=int(rng.integers(0, 25))).tolist()
+            segs.append(seg)
+            s.memory_append(seg)
+            assert s.memory() == OS.memory_array(segs, cap), cap
+        s.memory_clear()
+        assert s.memory() == []
+    with pytest.raises(W.W4A8Error):
+        _session(tiny).memory_append([1, 2])             # no memory in this session
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_draft_with_memory_matches_oracle(tiny, seed):
+    rng = np.random.default_rng(150 + seed)
+    motifs = rng.integers(0, 30, size=(4, 8))
+    def sample(n):
+        c = np.concatenate([motifs[i] for i in rng.integers(0, 4, size=n // 8 + 1)])[:n].copy()
+        sub = rng.random(n) < 0.25
+        c[sub] = rng.integers(0, 30, size=int(sub.sum()))
+        return c.tolist()
+    segs = [sample(int(rng.integers(1, 120))) for _ in range(int(rng.integers(1, 5)))]
+    ctx = sample(int(rng.integers(2, 200)))
+    s = _session(tiny, kv_cap=600, ctx_cap=1024, mem_cap=512)
+    for seg in segs:
+        s.memory_append(seg)
+    s.prefill(_dev(np.asarray(ctx, np.int32)), max_new=1)
+    tok, par, dep, n_valid, best = s.tree()
+    o_tok, o_par, o_nv, o_best = OS.draft(ctx, 16, memory=OS.memory_array(segs, 512))
+    assert (n_valid, best) == (o_nv, o_best)
+    assert tok[:n_valid] == o_tok[:n_valid].tolist() and par[1:n_valid] == o_par[1:n_valid].tolist()
+
+
+def test_memory_speculation_equals_greedy_and_takes_fewer_steps(tiny):
+    """A request whose answer is in the memory: drafts come from the memory, the output is still
+    the greedy output, and far fewer verification steps run."""
+    prompt = list(tiny["prompt"])
+    s = _session(tiny, mem_cap=4096)
+    greedy, rep_g = s.decode(prompt, 32, window=1, fixed_width=1, in_flight=1)
+    plain, rep_p = s.decode(prompt, 32, window=4, fixed_width=8, in_flight=2)
+    s.memory_append(greedy)
+    mem, rep_m = s.decode(prompt, 32, window=4, fixed_width=8, in_flight=2)
+    assert plain == greedy and mem == greedy
+    assert rep_m.n_steps < rep_p.n_steps
+    if greedy == tiny["greedy"]:   # the oracle's loop with the same memory takes the same steps
+        _, o_stats = OS.spec_decode(tiny["ow"], prompt, 32, 8, memory=OS.memory_array([greedy], 4096))
+        assert rep_m.n_steps == len(o_stats)
 
 
 def test_spec_steps_match_oracle_loop(tiny):

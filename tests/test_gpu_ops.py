@@ -169,3 +169,70 @@ def test_matmul_repeated_calls_reuse_workspace():
     ys = [W.w4a8_matmul(a_q, a_s, w_t, s_t, N, workspace=ws) for _ in range(4)]
     for y in ys[1:]:
         assert torch.equal(y, ys[0])
+
+
+# ------------------------------------------------------------- non-deterministic variant
+
+@pytest.mark.parametrize("M,K,N", [(1, 896, 4864), (8, 4864, 896), (16, 4096, 1024), (3, 14336, 256), (5, 96, 48)])
+def test_nondet_matmul_matches_oracle_within_the_same_bound(M, K, N):
+    # the same exact integer group sums and slice chains; only the order of the S slice adds
+    # differs, which the first-order bound (G + S + 2) 2^-24 sum|terms| already covers
+    seed = 2500 + M + K
+    q, s, x = synth.matmul_case(seed, M, K, N)
+    a_q, a_s = W.w4a8_quantize_rows(_to_dev(x), 0)
+    w_t, s_t = _gpu_weights(q, s)
+    y = W.w4a8_matmul_nondet(a_q, a_s, w_t, s_t, N).cpu().numpy().astype(np.float64)
+    a_q_ref, a_s_ref = Q.quantize_act_per_token(x)
+    ref = OMM.w4a8_matmul(a_q_ref, a_s_ref, Q.pack_q4(q), s)
+    tol = _tol(a_q_ref, a_s_ref, q, s, K, N)
+    assert np.all(np.abs(y - ref) <= tol), float(np.max(np.abs(y - ref) / tol))
+    if W.w4a8_matmul_slices(K, N) == 1:   # a single slice: nothing to reorder, same bits
+        assert np.array_equal(y, W.w4a8_matmul(a_q, a_s, w_t, s_t, N).cpu().numpy().astype(np.float64))
+
+
+# ------------------------------------------------------------------ per-32 activation scales
+
+def _per32_case(seed, M, K, N):
+    q, s, x = synth.matmul_case(seed, M, K, N)
+    xd = _to_dev(x)
+    a_q, a_s = W.w4a8_quantize_rows(xd, 1)              # one scale per block of 32 inputs
+    a_q_ref, a_s_ref = Q.quantize_act_per_block32(x)
+    assert np.array_equal(a_q.cpu().numpy(), a_q_ref) and np.array_equal(a_s.cpu().numpy(), a_s_ref)
+    return q, s, a_q, a_s, a_q_ref, a_s_ref
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 896, 4864), (8, 4864, 896), (16, 4096, 1024), (5, 704, 512), (3, 96, 48)])
+def test_per32_matmul_matches_oracle(M, K, N):
+    q, s, a_q, a_s, a_q_ref, a_s_ref = _per32_case(5000 + M + K, M, K, N)
+    w_t, s_t = _gpu_weights(q, s)
+    y = W.w4a8_matmul_per32(a_q, a_s, w_t, s_t, N).cpu().numpy().astype(np.float64)
+    ref = OMM.w4a8_matmul(a_q_ref, a_s_ref, Q.pack_q4(q), s)
+    # one more rounding than the per-token form: the product scale s_w * s_a of each group
+    G = K // 32
+    tol = (G + W.w4a8_matmul_slices(K, N) + 3) * 2.0 ** -24 * OMM.abs_terms(a_q_ref, a_s_ref, q, s) + 1e-30
+    assert np.all(np.abs(y - ref) <= tol), float(np.max(np.abs(y - ref) / tol))
+
+
+def test_per32_matmul_m_tokens_bitwise_equal_single_token_calls():
+    M, K, N = 16, 4864, 896
+    q, s, a_q, a_s, _, _ = _per32_case(5100, M, K, N)
+    w_t, s_t = _gpu_weights(q, s)
+    y_all = W.w4a8_matmul_per32(a_q, a_s, w_t, s_t, N)
+    for t in (0, 5, 8, 15):
+        y1 = W.w4a8_matmul_per32(a_q[t:t + 1].contiguous(), a_s[t:t + 1].contiguous(), w_t, s_t, N)
+        assert torch.equal(y1[0], y_all[t])
+
+
+def test_per32_with_equal_block_scales_is_the_per_token_product():
+    # every block of a row with the per-token scale: the same products, the per-32 order
+    # multiplies the scale into each group instead of the fold, so agreement is to rounding
+    M, K, N = 4, 4096, 512
+    q, s, x = synth.matmul_case(5200, M, K, N)
+    a_q, a_s = W.w4a8_quantize_rows(_to_dev(x), 0)
+    a_s32 = a_s[:, None].expand(M, K // 32).contiguous()
+    w_t, s_t = _gpu_weights(q, s)
+    y_tok = W.w4a8_matmul(a_q, a_s, w_t, s_t, N).cpu().numpy().astype(np.float64)
+    y_32 = W.w4a8_matmul_per32(a_q, a_s32, w_t, s_t, N).cpu().numpy().astype(np.float64)
+    a_q_ref, a_s_ref = Q.quantize_act_per_token(x)
+    tol = 2 * (K // 32 + W.w4a8_matmul_slices(K, N) + 3) * 2.0 ** -24 * OMM.abs_terms(a_q_ref, a_s_ref, q, s)
+    assert np.all(np.abs(y_32 - y_tok) <= tol)

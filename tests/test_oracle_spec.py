@@ -328,3 +328,65 @@ def test_draft_score_outranks_depth():
     tok, parent, n_valid, best = OS.draft(ctx, 3)
     # Q (score 2, depth 2) before S (score 1, depth 1)
     assert best == 2 and tok[1:3].tolist() == [P, Q] and parent[1:3].tolist() == [0, 1]
+
+
+# ------------------------------------------------------------------ session memory pins
+# Draft-Free Drafting From Web Context: a memory region holds earlier outputs and the same scan
+# searches it.  Reading: outputs are separated by SEP, a match or a continuation never crosses a
+# SEP, and the memory counts as older than the context.
+
+def test_memory_array_keeps_whole_recent_outputs():
+    S = OS.SEP
+    assert OS.memory_array([[1, 2], [3]]) == [S, 1, 2, S, 3]
+    assert OS.memory_array([[1, 2, 3], [4, 5], [6]], cap=6) == [S, 4, 5, S, 6]   # oldest output dropped
+    assert OS.memory_array([list(range(10))], cap=5) == [S, 6, 7, 8, 9]           # last cap - 1 tokens
+    assert OS.memory_array([]) == []
+
+
+def _brute_mem_ell(mem, ctx, v, max_order=8):
+    seq = mem + ctx
+    m = len(mem)
+    lo = 0 if v < m else m                     # a match stays inside the memory or the context
+    best = 0
+    for l in range(1, max_order + 1):
+        if v - l + 1 < lo or l > len(ctx):
+            break
+        if seq[v - l + 1:v + 1] == ctx[len(ctx) - l:]:
+            best = l
+    return best
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_memory_match_lengths_brute_force(seed):
+    rng = np.random.default_rng(700 + seed)
+    segs = [rng.integers(0, 3, size=int(rng.integers(1, 12))).tolist() for _ in range(int(rng.integers(0, 4)))]
+    mem = OS.memory_array(segs)
+    ctx = rng.integers(0, 3, size=int(rng.integers(2, 30))).tolist()
+    ell = OS.match_lengths_with_memory(mem, ctx)
+    assert ell.tolist() == [_brute_mem_ell(mem, ctx, v) for v in range(len(mem) + len(ctx) - 1)]
+
+
+def test_memory_only_match_drafts_its_continuation_up_to_the_separator():
+    mem = OS.memory_array([[50, 51, 52, 53], [60, 61]])
+    tok, parent, n_valid, best = OS.draft([7, 8, 51], 8, memory=mem)
+    assert best == 1 and n_valid == 3 and tok[1:3].tolist() == [52, 53]        # stops at the SEP before 60
+    assert parent[1:3].tolist() == [0, 1]
+    tok, _, n_valid, _ = OS.draft([7, 8, 51], 8)                                # no memory: nothing to draft
+    assert n_valid == 1
+
+
+def test_memory_match_does_not_cross_an_output_boundary():
+    mem = OS.memory_array([[9], [5, 6]])                     # [SEP, 9, SEP, 5, 6]
+    ell = OS.match_lengths_with_memory(mem, [1, 9, 5])
+    assert ell[3] == 1                                       # 5 is preceded by SEP, not by 9
+
+
+def test_context_is_more_recent_than_memory_at_equal_length():
+    R = 40
+    mem = OS.memory_array([[R, 41]])
+    tok, _, _, best = OS.draft([R, 42, 3, R], 2, memory=mem)
+    assert best == 1 and tok[1] == 42
+    # a longer match in the memory outranks a shorter one in the context
+    mem = OS.memory_array([[77, R, 41]])
+    tok, _, _, best = OS.draft([R, 42, 3, 77, R], 2, memory=mem)
+    assert best == 2 and tok[1] == 41

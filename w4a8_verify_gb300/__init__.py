@@ -26,7 +26,7 @@ class ModelDesc(_c.Structure):
 
 
 class SessionDesc(_c.Structure):
-    _fields_ = [("kv_cap", _i32), ("ctx_cap", _i32), ("max_window", _i32), ("eos_id", _i32)]
+    _fields_ = [("kv_cap", _i32), ("ctx_cap", _i32), ("max_window", _i32), ("eos_id", _i32), ("mem_cap", _i32)]
 
 
 class Ctl(_c.Structure):
@@ -70,6 +70,8 @@ _SIGNATURES = {
     "w4a8_matmul": [_vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp],
     "w4a8_matmul_slices": [_i32, _i32],
     "w4a8_matmul_inject_timeout": [_vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp],
+    "w4a8_matmul_nondet": [_vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp],
+    "w4a8_matmul_per32": [_vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp],
     "w4a8_matmul_check": [_vp, _i32, _i32, _i32, _c.POINTER(_c.c_uint32)],
     "w4a8_matmul_noalloc": [_vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp],
     "w4a8_matmul_noalloc_check": [_c.POINTER(_c.c_uint32)],
@@ -106,6 +108,9 @@ _SIGNATURES = {
     "w4a8_session_copy_kv": [_vp, _i32, _i32, _i32, _vp, _vp, _vp],
     "w4a8_session_load_kv": [_vp, _i32, _i32, _i32, _vp, _vp, _vp],
     "w4a8_session_attention": [_vp, _i32, _i32, _vp, _vp, _vp],
+    "w4a8_session_memory_append": [_vp, _c.POINTER(_i32), _i32],
+    "w4a8_session_memory_clear": [_vp],
+    "w4a8_session_memory_get": [_vp, _c.POINTER(_i32), _i32, _c.POINTER(_i32)],
     "w4a8_controller_create": [_c.POINTER(_i32), _c.POINTER(_f32), _i32, _c.POINTER(_vp)],
     "w4a8_controller_destroy": [_vp],
     "w4a8_controller_choose": [_vp],
@@ -242,6 +247,34 @@ def w4a8_matmul_noalloc(a_q, a_s, w_t, s_t, N, y, stream=None):
     return y
 
 
+def w4a8_matmul_per32(a_q, a_s, w_t, s_t, N, y=None, workspace=None, stream=None):
+    """W4A8 product with per-32 activation scales a_s [M][K/32] (w4a8_matmul_per32)."""
+    import torch
+    M, K = a_q.shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=a_q.device)
+    need = w4a8_matmul_workspace_bytes(M, K, N)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=a_q.device)
+    _call("w4a8_matmul_per32", _ptr(a_q), _ptr(a_s), M, K, _ptr(w_t), _ptr(s_t), N, _ptr(y), _ptr(workspace),
+          workspace.numel() * workspace.element_size(), _stream(stream))
+    return y
+
+
+def w4a8_matmul_nondet(a_q, a_s, w_t, s_t, N, y=None, workspace=None, stream=None):
+    """The non-deterministic fast variant (slices combined with float atomics)."""
+    import torch
+    M, K = a_q.shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=a_q.device)
+    need = w4a8_matmul_workspace_bytes(M, K, N)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=a_q.device)
+    _call("w4a8_matmul_nondet", _ptr(a_q), _ptr(a_s), M, K, _ptr(w_t), _ptr(s_t), N, _ptr(y), _ptr(workspace),
+          workspace.numel() * workspace.element_size(), _stream(stream))
+    return y
+
+
 def w4a8_matmul_inject_timeout(a_q, a_s, w_t, s_t, N, y, workspace, stream=None):
     """Test-only: the matmul with a copy warp that issues nothing, so that its bounded waits
     expire and the workspace status word reports the timeout (w4a8_matmul_inject_timeout)."""
@@ -314,9 +347,9 @@ class Model:
 class Session:
     """A decoding session (w4a8_session) on a Model."""
 
-    def __init__(self, model, kv_cap, ctx_cap, max_window=16, eos_id=-1):
+    def __init__(self, model, kv_cap, ctx_cap, max_window=16, eos_id=-1, mem_cap=0):
         self.model = model
-        self.desc = SessionDesc(kv_cap, ctx_cap, max_window, eos_id)
+        self.desc = SessionDesc(kv_cap, ctx_cap, max_window, eos_id, mem_cap)
         h = _vp()
         _call("w4a8_session_create", model.h, _c.byref(self.desc), _c.byref(h))
         self.h = h
@@ -451,6 +484,19 @@ class Session:
     def copy_kv(self, layer, slot0, n, k_out, v_out, stream=None):
         _call("w4a8_session_copy_kv", self.h, int(layer), int(slot0), int(n), _ptr(k_out), _ptr(v_out),
               _stream(stream))
+
+    def memory_append(self, tokens):
+        """Appends an earlier output to the session memory (w4a8_session_memory_append)."""
+        _call("w4a8_session_memory_append", self.h, _arr([int(t) for t in tokens]), len(tokens))
+
+    def memory_clear(self):
+        _call("w4a8_session_memory_clear", self.h)
+
+    def memory(self, cap=1 << 16):
+        out = (_i32 * cap)()
+        n = _i32()
+        _call("w4a8_session_memory_get", self.h, out, cap, _c.byref(n))
+        return list(out)[:min(cap, n.value)]
 
     def load_kv(self, layer, slot0, n, k_in, v_in, stream=None):
         _call("w4a8_session_load_kv", self.h, int(layer), int(slot0), int(n), _ptr(k_in), _ptr(v_in),

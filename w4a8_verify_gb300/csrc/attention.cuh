@@ -144,7 +144,21 @@ __global__ void __maxnreg__(168)
   __shared__ uint64_t full[NE], empty[NE];
   __shared__ unsigned s_last;
   const int kh = blockIdx.y;
-  const int L = (int)ctl->committed_len;
+  // blockIdx.z: 16-node sub-chain of a prefill bucket (0 in verification).  Sub-chain j is the
+  // chain of the bucket's tokens 16j .. 16j+15: its committed length is 16j further, and its
+  // queries, outputs and partials are the next 16 rows of each buffer.  Only the variants that
+  // leave the merge to k_attn_merge take prefill buckets (16-node chains with G >= 2).
+  const int sub = MERGE ? 0 : (int)blockIdx.z;
+  if (sub > 0) {
+    const size_t rows = (size_t)sub * kMaxWidth;
+    qrot += rows * Hq * D;
+    out += rows * Hq * D;
+    mpart += rows * Hq;
+    o_part += rows * gridDim.x * Hq * D;
+    ml_part += rows * gridDim.x * Hq;
+    tickets += (size_t)sub * gridDim.y;
+  }
+  const int L = (int)ctl->committed_len + sub * kMaxWidth;
   int maxd = 0;
   for (int i = 0; i < N; ++i) maxd = max(maxd, tree->depth[i]);
   const int nch = (L + maxd) / CH + 1;
@@ -182,6 +196,9 @@ __global__ void __maxnreg__(168)
     // each (rows land at the padded strides; columns past D and rows past the cache read zero;
     // rows between L and the chunk end are never read from the ring)
     if (lane == 0) {
+      // a later sub-chain's cached rows include the rows the kernel just before this one wrote
+      // for the earlier sub-chains of the bucket: wait for it before the first copy
+      if (sub > 0) griddep_wait();
       int n = 0;  // entries issued
       for (int c = c_begin; c < c_end; ++c) {
         const int P0 = c * CH;
@@ -788,8 +805,8 @@ __global__ void __maxnreg__(168)
 
 // Merge of the split partials for wide trees (defined in layers.cu).
 __global__ void k_attn_merge(const SpecCtl* ctl, const TreeState* __restrict__ tree, const float* __restrict__ o_part,
-                             const float2* __restrict__ ml_part, int Hq, int D, int R, float* __restrict__ out,
-                             float2* __restrict__ mpart);
+                             const float2* __restrict__ ml_part, int Hq, int D, int R, int splits,
+                             float* __restrict__ out, float2* __restrict__ mpart);
 
 // Launch templates: every (G, QT) variant of head size D is configured up front; a launch picks
 // the variant for N.
@@ -812,13 +829,19 @@ cudaError_t attn_launch(bool configure, size_t smem, const DecoderBufs& b, const
   const float* vc = b.vcache + layer * lstride;
   const int splits = min(attn_splits(m.Hkv), b.n_chunks);
   const int R = (b.n_chunks + splits - 1) / splits;  // chunks per split (fixed per session)
-  cudaError_t e = launch_pdl(k_attn<D, G, QT, MERGE>, dim3(splits, m.Hkv), dim3(kAttnThreads),
-                             attn_smem_bytes(D, N * G), st, b.ctl, (const TreeState*)b.tree, N, (const float*)b.qrot,
+  // more than kMaxWidth rows: a prefill bucket, N / kMaxWidth chains of kMaxWidth nodes (variants
+  // that merge inside the kernel take one chain)
+  const int nsub = N > kMaxWidth ? N / kMaxWidth : 1;
+  const int Nn = N > kMaxWidth ? kMaxWidth : N;
+  if (MERGE && nsub > 1) return cudaErrorInvalidValue;
+  cudaError_t e = launch_pdl(k_attn<D, G, QT, MERGE>, dim3(splits, m.Hkv, nsub), dim3(kAttnThreads),
+                             attn_smem_bytes(D, Nn * G), st, b.ctl, (const TreeState*)b.tree, Nn, (const float*)b.qrot,
                              kc, vc, b.kv_cap, m.Hq, R, b.o_part, (float2*)b.ml_part, b.attn_tickets, b.qkv, b.qpart,
                              b.tm_k, b.tm_v, layer);
   if (e != cudaSuccess || MERGE) return e;
-  return launch_pdl(k_attn_merge, dim3(N, m.Hq), dim3(m.D), 0, st, (const SpecCtl*)b.ctl, (const TreeState*)b.tree,
-                    (const float*)b.o_part, (const float2*)b.ml_part, m.Hq, m.D, R, b.qkv, b.qpart);
+  return launch_pdl(k_attn_merge, dim3(Nn * nsub, m.Hq), dim3(m.D), 0, st, (const SpecCtl*)b.ctl,
+                    (const TreeState*)b.tree, (const float*)b.o_part, (const float2*)b.ml_part, m.Hq, m.D, R, splits,
+                    b.qkv, b.qpart);
 }
 // QT: queries per compute warp, the power of two >= ceil(N*G / 8) (every variant is
 // configured up front; launching picks the one for N)
@@ -826,7 +849,8 @@ template <int D, int G>
 cudaError_t attn_dispatch(bool configure, size_t smem, const DecoderBufs& b, const ModelDims& m, int N, int layer,
                           cudaStream_t st) {
   constexpr int QTMAX = (kMaxWidth * G + kAttnWarps - 1) / kAttnWarps;
-  const int qt = configure ? 1 : (N * G + kAttnWarps - 1) / kAttnWarps;
+  const int Nn = N > kMaxWidth ? kMaxWidth : N;  // nodes per (sub-)chain
+  const int qt = configure ? 1 : (Nn * G + kAttnWarps - 1) / kAttnWarps;
   cudaError_t e = cudaSuccess;
   if (configure || qt <= 1) e = attn_launch<D, G, 1>(configure, smem, b, m, N, layer, st);
   if constexpr (QTMAX > 1)

@@ -10,6 +10,7 @@
 namespace w4a8 {
 
 constexpr int kMaxWidth = 16;     // tree nodes per step (node 0 = last committed token)
+constexpr int kMaxBucket = 32;    // prompt tokens per prefill bucket (two chains of kMaxWidth for attention)
 constexpr int kMaxCont = 8;       // drafter continuation length -> at most 9 tokens per step
 constexpr int kAttnChunk = 64;    // logical positions per attention chunk (fixed: part of the order)
 
@@ -68,27 +69,29 @@ struct DecoderBufs {
   AcceptRec* rec;
   int32_t* ctx;
   int32_t* pred;          // [16]
-  float* x;               // [16][H] residual stream
-  float* qkv;             // [16][qkv_rows]
-  float* qrot;            // [16][Hq][D]
-  float* gu;              // [16][2F]
+  float* x;               // [kMaxBucket][H] residual stream
+  float* qkv;             // [kMaxBucket][qkv_rows] (the attention output [kMaxBucket][Hq*D] too)
+  float* qrot;            // [kMaxBucket][Hq][D]
+  float* gu;              // [kMaxBucket][2F]
   float* logits;          // [16][V]
-  float* o_part;          // attention split partials [split][16][Hq][D] (split < n_chunks)
-  float* ml_part;         // [split][16][Hq] (running max, sum)
+  float* o_part;          // attention split partials [chain][split][16][Hq][D] (split < n_chunks, 2 chains)
+  float* ml_part;         // [chain][split][16][Hq] (running max, sum)
   uint8_t* act;           // activation records of the next matmul (max K)
-  float* a_s;             // [16] activation scales
+  float* a_s;             // [kMaxBucket] activation scales
   float* mm_part;         // split-K partials
   unsigned* tickets;      // split-K counters (zero between kernels)
   float* kcache;          // [L][Hkv][kv_cap][D]
   float* vcache;
   float2* rope;           // [kv_cap][D/2] (cos, sin)
-  float2* qpart;          // [16][slices] (sum of squares, max |x|) partials of the quantisation passes
+  float2* qpart;          // [kMaxBucket][slices] (sum of squares, max |x|) partials of the quantisation passes
   float2* argmax_part;    // [16][vocab slices] (value, index) partials
   unsigned* argmax_tickets;  // [16], zero between kernels
-  unsigned* attn_tickets;    // [Hkv], zero between kernels
+  unsigned* attn_tickets;    // [2 chains][Hkv], zero between kernels
+  int32_t* mem;           // [mem_cap] session memory: earlier outputs, each preceded by -1
+  int* mem_len;           // entries of mem in use (device word, read by the drafter)
   StepStats* wstats;      // [max_window] current window's statistics
   int32_t* wtok;          // [max_window][16] emitted tokens per step of the window
-  int kv_cap, ctx_cap, n_chunks, max_window;
+  int kv_cap, ctx_cap, n_chunks, max_window, mem_cap;
   int eos_id;
   // TMA maps of the K and V caches, dims {D, kv_cap, Hkv, layers}; a box is one attention
   // chunk of 64 rows landing at the padded shared-memory row strides

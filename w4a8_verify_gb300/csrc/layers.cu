@@ -27,8 +27,11 @@ constexpr int kQuantSlice = 512;  // inputs per CTA of the statistics and quanti
 
 // ------------------------------------------------------------------------------ embedding
 
-__global__ void k_embed(SpecCtl* ctl, const TreeState* __restrict__ tree, int N, const uint32_t* __restrict__ ew,
-                        const uint16_t* __restrict__ es, int H, int V, int kv_cap, float* __restrict__ x) {
+// Token i of the pass: tree node i, or (chain != nullptr: a prefill bucket) context token
+// committed_len + i.
+__global__ void k_embed(SpecCtl* ctl, const TreeState* __restrict__ tree, const int32_t* __restrict__ chain, int N,
+                        const uint32_t* __restrict__ ew, const uint16_t* __restrict__ es, int H, int V, int kv_cap,
+                        float* __restrict__ x) {
   griddep_enter();
   if (stopped(ctl)) return;
   const int i = blockIdx.x;
@@ -37,7 +40,7 @@ __global__ void k_embed(SpecCtl* ctl, const TreeState* __restrict__ tree, int N,
     if (i == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(&ctl->flags, FLAG_ERR_CAPACITY);
     return;
   }
-  const int tok = tree->tok[i];
+  const int tok = chain != nullptr ? chain[L + i] : tree->tok[i];
   if (tok < 0 || tok >= V) {
     if (blockIdx.y == 0 && threadIdx.x == 0) atomicOr(&ctl->flags, FLAG_ERR_TOKEN);
     return;
@@ -161,15 +164,16 @@ __global__ void k_quant_slices(const SpecCtl* ctl, const float* __restrict__ x, 
 
 // grid (node, head among Hq query + Hkv key + Hkv value heads), D/2 threads
 // The projection's output rows come from its EPI_PARTIAL slices (folded here).
-__global__ void k_rope_kv(const SpecCtl* ctl, const TreeState* __restrict__ tree, const float* __restrict__ qkv_part,
-                          int qkv_S, const float* __restrict__ a_s, int Hq, int Hkv, int D,
-                          const float2* __restrict__ rope, float* kc, float* vc, int kv_cap,
+// chain != 0 (a prefill bucket): token i sits at position committed_len + i.
+__global__ void k_rope_kv(const SpecCtl* ctl, const TreeState* __restrict__ tree, int chain,
+                          const float* __restrict__ qkv_part, int qkv_S, const float* __restrict__ a_s, int Hq, int Hkv,
+                          int D, const float2* __restrict__ rope, float* kc, float* vc, int kv_cap,
                           float* __restrict__ qrot, float qscale) {
   griddep_enter();
   if (stopped(ctl)) return;
   const int i = blockIdx.x, h = blockIdx.y, j = threadIdx.x;
   const int L = (int)ctl->committed_len;
-  const int pos = L + tree->depth[i];
+  const int pos = L + (chain ? i : tree->depth[i]);
   const int slot = L + i;
   const int half = D / 2;
   const int rows = (Hq + 2 * Hkv) * D;
@@ -197,15 +201,20 @@ __global__ void k_rope_kv(const SpecCtl* ctl, const TreeState* __restrict__ tree
 // Merge of the split partials for wide trees: grid (node, query head), one thread per
 // dimension; the same order and operations as the in-kernel merge of k_attn.
 __global__ void k_attn_merge(const SpecCtl* ctl, const TreeState* __restrict__ tree, const float* __restrict__ o_part,
-                             const float2* __restrict__ ml_part, int Hq, int D, int R, float* __restrict__ out,
-                             float2* __restrict__ mpart) {
+                             const float2* __restrict__ ml_part, int Hq, int D, int R, int splits,
+                             float* __restrict__ out, float2* __restrict__ mpart) {
   griddep_enter();
   if (stopped(ctl)) return;
   __shared__ float s_mx[4];
-  const int i = blockIdx.x, h = blockIdx.y, dd = threadIdx.x;
-  const int L = (int)ctl->committed_len;
+  // row it = node i of sub-chain sub (prefill buckets hold several chains of kMaxWidth nodes)
+  const int it = blockIdx.x, h = blockIdx.y, dd = threadIdx.x;
+  const int sub = it / kMaxWidth, i = it - sub * kMaxWidth;
+  o_part += (size_t)sub * kMaxWidth * splits * Hq * D;
+  ml_part += (size_t)sub * kMaxWidth * splits * Hq;
+  const int L = (int)ctl->committed_len + sub * kMaxWidth;
   const int smax = ((L + tree->depth[i]) / kAttnChunk) / R;
   const size_t hb = (size_t)i * Hq + h;
+  const size_t ho = (size_t)it * Hq + h;
   const size_t sstride = (size_t)kMaxWidth * Hq;
   float M = -INFINITY;
   for (int s2 = 0; s2 <= smax; ++s2) M = fmaxf(M, ml_part[s2 * sstride + hb].x);
@@ -228,14 +237,14 @@ __global__ void k_attn_merge(const SpecCtl* ctl, const TreeState* __restrict__ t
     }
   }
   const float res = __fdiv_rn(O, Ls);
-  out[hb * D + dd] = res;
+  out[ho * D + dd] = res;
   const float mx = warp_max(fabsf(res));
   if ((dd & 31) == 0) s_mx[dd >> 5] = mx;
   __syncthreads();
   if (dd == 0) {
     float m = s_mx[0];
     for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, s_mx[w]);
-    mpart[hb] = make_float2(0.0f, m);
+    mpart[ho] = make_float2(0.0f, m);
   }
 }
 
@@ -398,11 +407,10 @@ cudaError_t attn_configure(const ModelDims& m, size_t smem) {
   return attn_any(m.D, m.Hq / m.Hkv, true, smem, b, m, 1, 0, nullptr);
 }
 
-cudaError_t launch_embed(const DecoderBufs& b, const ModelDims& m, int N, const uint32_t* ew, const uint16_t* es,
-                         cudaStream_t st) {
-  return launch_pdl(k_embed, dim3(N, (m.H / 8 + 127) / 128), dim3(128), 0, st, b.ctl, (const TreeState*)b.tree, N, ew,
-                    es, m.H, m.V,
-                    b.kv_cap, b.x);
+cudaError_t launch_embed(const DecoderBufs& b, const ModelDims& m, int N, bool chain, const uint32_t* ew,
+                         const uint16_t* es, cudaStream_t st) {
+  return launch_pdl(k_embed, dim3(N, (m.H / 8 + 127) / 128), dim3(128), 0, st, b.ctl, (const TreeState*)b.tree,
+                    chain ? (const int32_t*)b.ctx : nullptr, N, ew, es, m.H, m.V, b.kv_cap, b.x);
 }
 
 cudaError_t launch_rmsnorm_quant(const DecoderBufs& b, const ModelDims& m, int N, const float* res, int res_S,
@@ -415,18 +423,21 @@ cudaError_t launch_rmsnorm_quant(const DecoderBufs& b, const ModelDims& m, int N
                     (const float*)b.x, m.H, m.H, (const float2*)b.qpart, ns, m.eps, b.act, N, b.a_s);
 }
 
-cudaError_t launch_rope_kv(const DecoderBufs& b, const ModelDims& m, int N, int layer, int qkv_S, cudaStream_t st) {
+cudaError_t launch_rope_kv(const DecoderBufs& b, const ModelDims& m, int N, bool chain, int layer, int qkv_S,
+                           cudaStream_t st) {
   const size_t lstride = (size_t)m.Hkv * b.kv_cap * m.D;
   const float qscale = (float)(1.0 / sqrt((double)m.D));
   return launch_pdl(k_rope_kv, dim3(N, m.Hq + 2 * m.Hkv), dim3(m.D / 2), 0, st, (const SpecCtl*)b.ctl,
-                    (const TreeState*)b.tree, (const float*)b.mm_part, qkv_S, (const float*)b.a_s, m.Hq, m.Hkv, m.D,
+                    (const TreeState*)b.tree, chain ? 1 : 0, (const float*)b.mm_part, qkv_S, (const float*)b.a_s, m.Hq,
+                    m.Hkv, m.D,
                     (const float2*)b.rope, b.kcache + layer * lstride,
                     b.vcache + layer * lstride, b.kv_cap, b.qrot, qscale);
 }
 
 cudaError_t launch_attention(const DecoderBufs& b, const ModelDims& m, int N, int layer, cudaStream_t st) {
   const int G = m.Hq / m.Hkv;
-  cudaError_t e = attn_any(m.D, G, false, attn_smem_bytes(m.D, N * G), b, m, N, layer, st);
+  const int Nn = N > kMaxWidth ? kMaxWidth : N;  // a prefill bucket runs as chains of kMaxWidth nodes
+  cudaError_t e = attn_any(m.D, G, false, attn_smem_bytes(m.D, Nn * G), b, m, N, layer, st);
   if (e != cudaSuccess) return e;
   // the attention output (in the qkv buffer, [N][Hq*D]) -> int8 fragments of the O projection
   const int QD = m.Hq * m.D;

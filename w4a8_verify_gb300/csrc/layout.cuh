@@ -15,7 +15,7 @@
 // 16n * 2^-24.  Pairs p = 1, 3 carry the extra factor 16, which the activation side
 // cancels by holding a/16 for those inputs.
 //
-// Activation records.  For NT 8-token tiles (NT = 1 for up to 8 tokens, else 2) the
+// Activation records.  For NT 8-token tiles (NT = 1 for up to 8 tokens, 2 up to 16, 4 up to 32) the
 // record of chunk c is NT * 1152 bytes at offset c * NT * 1152:
 //   [nt][group 0..1][lane] uint4 {h2(a_k, a_k+1), h2(a_k+8, a_k+9)/16,
 //                                h2(a_k+16, a_k+17), h2(a_k+24, a_k+25)/16},
@@ -45,9 +45,11 @@ __host__ __device__ inline size_t tile_index(int N, int KC, int rb, int c) {
   return (size_t)grp * kGroupBlocks * KC + (size_t)c * nrb + rbl;
 }
 
-// activation records: 8-token tiles for M tokens, bytes per chunk, buffer bytes for K inputs
-__host__ __device__ inline int act_tiles(int M) { return M > 8 ? 2 : 1; }
+// activation records: 8-token tiles for M tokens (1, 2 or 4 tiles: up to 32 tokens), bytes per
+// chunk, buffer bytes for K inputs (act_bytes: up to 16 tokens; act_bytes_nt: NT tiles)
+__host__ __device__ inline int act_tiles(int M) { return M > 16 ? 4 : (M > 8 ? 2 : 1); }
 __host__ __device__ inline int act_rec_bytes(int NT) { return NT * 1152; }
 __host__ __device__ inline size_t act_bytes(int K) { return (size_t)chunks_of(K) * 2 * 1152; }
+__host__ __device__ inline size_t act_bytes_nt(int K, int NT) { return (size_t)chunks_of(K) * NT * 1152; }
 
 }  // namespace w4a8

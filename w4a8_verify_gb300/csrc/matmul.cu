@@ -77,6 +77,25 @@ __device__ __forceinline__ void fma2(float& c0, float& c1, float a, float b0, fl
   c1 = __uint_as_float((uint32_t)(c >> 32));
 }
 
+// (c0, c1) = (a0 * b0 + c0, a1 * b1 + c1) in one packed instruction (two fmaf).
+__device__ __forceinline__ void fma2v(float& c0, float& c1, float a0, float a1, float b0, float b1) {
+  uint64_t c = ((uint64_t)__float_as_uint(c1) << 32) | __float_as_uint(c0);
+  const uint64_t aa = ((uint64_t)__float_as_uint(a1) << 32) | __float_as_uint(a0);
+  const uint64_t bb = ((uint64_t)__float_as_uint(b1) << 32) | __float_as_uint(b0);
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(c) : "l"(aa), "l"(bb));
+  c0 = __uint_as_float((uint32_t)c);
+  c1 = __uint_as_float((uint32_t)(c >> 32));
+}
+// (p0, p1) = (a * b0, a * b1), each rounded once, in one packed instruction.
+__device__ __forceinline__ void mul2(float& p0, float& p1, float a, float b0, float b1) {
+  const uint64_t aa = ((uint64_t)__float_as_uint(a) << 32) | __float_as_uint(a);
+  const uint64_t bb = ((uint64_t)__float_as_uint(b1) << 32) | __float_as_uint(b0);
+  uint64_t p;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p) : "l"(aa), "l"(bb));
+  p0 = __uint_as_float((uint32_t)p);
+  p1 = __uint_as_float((uint32_t)(p >> 32));
+}
+
 // The four A-fragment registers of one weight word (see layout.cuh).
 __device__ __forceinline__ void unpack_codes(uint32_t x, uint32_t (&r)[4]) {
   r[0] = x & 0x000F000Fu;
@@ -95,18 +114,30 @@ constexpr int kChunkW = kRowBlocksPerCta * 512;
 constexpr int kChunkS = kRowBlocksPerCta * 64;
 constexpr int kStageS0 = kChunkBatch * kChunkW;
 constexpr int kStageA0 = kStageS0 + kChunkBatch * kChunkS;
-constexpr int kStageBytes = kStageA0 + kChunkBatch * 2 * 1152;
+// Kernel modes: the production kernel, the test-only timeout variant, and per-32 activation
+// scales (one scale per token and group of 32 inputs, carried by the activation records).
+enum : int { kModeNormal = 0, kModeFault = 1, kModePer32 = 2 };
+// activation record bytes per 64-input chunk of one 8-token tile
+template <int MODE> constexpr int rec_tile_bytes() { return MODE == kModePer32 ? 1216 : 1152; }
+// a stage holds the records of at least two token tiles (the 1..16-token kernels share one size)
+template <int NT, int MODE = kModeNormal> constexpr int stage_bytes() {
+  return kStageA0 + kChunkBatch * (NT > 2 ? NT : 2) * rec_tile_bytes<MODE>();
+}
 constexpr int kStages = 4;
 constexpr int kMmThreads = 32 * (kWarpsPerCta + 1);                  // + one producer warp
-constexpr size_t kMmSmem = (size_t)kStages * kStageBytes;
+template <int NT, int MODE = kModeNormal> constexpr size_t mm_smem() {
+  return (size_t)kStages * stage_bytes<NT, MODE>();
+}
 
 // NCH consecutive chunks of one stage for the kRowBlocksPerWarp row blocks from rl0.
 // Groups are folded into acc in ascending order.
-template <int NT, int NCH>
+// P32: the group's product scale is s_w * s_a[t][g] per token (rounded once), taken from the
+// record's per-group scales, instead of s_w alone.
+template <int NT, int NCH, bool P32 = false>
 __device__ __forceinline__ void mm_chunks(const uint8_t* stage, int u0, int rl0, int lane,
                                           float (&acc)[kRowBlocksPerWarp][NT][4]) {
   const int gid = lane >> 2, tig = lane & 3;
-  constexpr int rec = NT * 1152;
+  constexpr int rec = NT * (P32 ? 1216 : 1152);
 #pragma unroll
   for (int u = u0; u < u0 + NCH; ++u) {
     const uint8_t* sa = stage + kStageA0 + u * rec;
@@ -115,10 +146,12 @@ __device__ __forceinline__ void mm_chunks(const uint8_t* stage, int u0, int rl0,
     for (int gg = 0; gg < 2; ++gg) {
       uint4 bf[NT];
       float4 cq[NT];
+      float2 as2[NT];  // P32: s_a of tokens t0 and t0 + 1 for this group
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         bf[nt] = reinterpret_cast<const uint4*>(sa + (nt * 2 + gg) * 512)[lane];
         cq[nt] = reinterpret_cast<const float4*>(sa + NT * 1024 + (gg * NT + nt) * 64)[tig];
+        if (P32) as2[nt] = reinterpret_cast<const float2*>(sa + NT * 1152 + (gg * NT + nt) * 32)[tig];
       }
 #pragma unroll
       for (int r = 0; r < kRowBlocksPerWarp; ++r) {
@@ -139,8 +172,16 @@ __device__ __forceinline__ void mm_chunks(const uint8_t* stage, int u0, int rl0,
           mma_f16(d[nt], wa[2], wb[2], wa[3], wb[3], bf[nt].z, bf[nt].w, d[nt][0], d[nt][1], d[nt][2], d[nt][3]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          fma2(acc[r][nt][0], acc[r][nt][1], sg.x, d[nt][0], d[nt][1]);
-          fma2(acc[r][nt][2], acc[r][nt][3], sg.y, d[nt][2], d[nt][3]);
+          if (P32) {
+            float p0, p1, p2, p3;  // s_w * s_a per (row, token), each rounded once
+            mul2(p0, p1, sg.x, as2[nt].x, as2[nt].y);
+            mul2(p2, p3, sg.y, as2[nt].x, as2[nt].y);
+            fma2v(acc[r][nt][0], acc[r][nt][1], p0, p1, d[nt][0], d[nt][1]);
+            fma2v(acc[r][nt][2], acc[r][nt][3], p2, p3, d[nt][2], d[nt][3]);
+          } else {
+            fma2(acc[r][nt][0], acc[r][nt][1], sg.x, d[nt][0], d[nt][1]);
+            fma2(acc[r][nt][2], acc[r][nt][3], sg.y, d[nt][2], d[nt][3]);
+          }
         }
       }
     }
@@ -162,16 +203,18 @@ constexpr uint64_t kFaultWaitNs = 1000000ull;
 // FAULT (test-only instantiation, never used by the decoder or w4a8_matmul): the producer
 // issues no copy and the consumers' bounded waits use kFaultWaitNs, so the timeout path (status
 // flag, skipped output, no copy left in flight) runs without any fault or hang.
-template <int NT, bool FAULT>
+template <int NT, int MODE>
 __global__ void __launch_bounds__(kMmThreads)
     k_mm(const uint8_t* __restrict__ wt, const uint8_t* __restrict__ st, const uint8_t* __restrict__ act,
          const float* __restrict__ a_s, int M, int N, int ldy, int KC, int cps, int S, float* __restrict__ y,
          int epi, float* __restrict__ part, unsigned* __restrict__ tickets, unsigned* __restrict__ err,
          const unsigned* __restrict__ stop) {
+  constexpr bool FAULT = MODE == kModeFault;
+  constexpr bool P32 = MODE == kModePer32;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full[kStages], empty[kStages];
   __shared__ unsigned s_ticket;
-  constexpr int rec = NT * 1152;
+  constexpr int rec = NT * rec_tile_bytes<MODE>();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n16 = N / 16;
   const int n_rg = (n16 + kGroupBlocks - 1) / kGroupBlocks;
@@ -216,7 +259,7 @@ __global__ void __launch_bounds__(kMmThreads)
         batch_info(ps, g, cb, nc, nrb);
         const int stg = it % kStages;
         mbar_expect_tx(&full[stg], (unsigned)(nc * nrb * 576 + nc * rec));
-        uint8_t* s0 = smem + (size_t)stg * kStageBytes;
+        uint8_t* s0 = smem + (size_t)stg * stage_bytes<NT, MODE>();
         const size_t t0 = tile_index(N, KC, g * kGroupBlocks, cb);
         if (nrb == kGroupBlocks) {  // the stage is one contiguous range of each array
           bulk_g2s(s0, wt + t0 * 512, (unsigned)(nc * kChunkW), &full[stg]);
@@ -233,7 +276,7 @@ __global__ void __launch_bounds__(kMmThreads)
         int g, cb, nc, nrb;
         batch_info(ps, g, cb, nc, nrb);
         const int stg = it % kStages;
-        bulk_g2s(smem + (size_t)stg * kStageBytes + kStageA0, act + (size_t)cb * rec, (unsigned)(nc * rec),
+        bulk_g2s(smem + (size_t)stg * stage_bytes<NT, MODE>() + kStageA0, act + (size_t)cb * rec, (unsigned)(nc * rec),
                  &full[stg]);
       };
       Pos pro[kStages];
@@ -297,13 +340,13 @@ __global__ void __launch_bounds__(kMmThreads)
           ok = false;
         }
         if (!ok) continue;
-        const uint8_t* stage = smem + (size_t)stg * kStageBytes;
+        const uint8_t* stage = smem + (size_t)stg * stage_bytes<NT, MODE>();
         // warps past the last row block of a short row group compute on the gap (results
         // are not stored)
         if (c1 - (c0 + b * kChunkBatch) >= kChunkBatch)
-          mm_chunks<NT, kChunkBatch>(stage, 0, warp * kRowBlocksPerWarp, lane, acc);
+          mm_chunks<NT, kChunkBatch, P32>(stage, 0, warp * kRowBlocksPerWarp, lane, acc);
         else
-          mm_chunks<NT, 1>(stage, 0, warp * kRowBlocksPerWarp, lane, acc);
+          mm_chunks<NT, 1, P32>(stage, 0, warp * kRowBlocksPerWarp, lane, acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stg]);
       }
@@ -320,7 +363,24 @@ __global__ void __launch_bounds__(kMmThreads)
               const int t = nt * 8 + 2 * tig + (e & 1);
               if (t >= M) continue;
               const int row = (rb0 + r) * 16 + gid + ((e & 2) ? 8 : 0);
-              part[((size_t)sl * 16 + t) * N + row] = acc[r][nt][e];
+              part[((size_t)sl * kPartTokens + t) * N + row] = acc[r][nt][e];
+            }
+        }
+        continue;
+      }
+      if (epi == EPI_ATOMIC) {
+        if (!ok) continue;
+#pragma unroll
+        for (int r = 0; r < kRowBlocksPerWarp; ++r) {
+          if (rb0 + r >= n16) continue;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int t = nt * 8 + 2 * tig + (e & 1);
+              if (t >= M) continue;
+              const int row = (rb0 + r) * 16 + gid + ((e & 2) ? 8 : 0);
+              atomicAdd(y + (size_t)t * ldy + row, acc[r][nt][e] * (P32 ? 16777216.0f : 16777216.0f * __ldg(a_s + t)));
             }
         }
         continue;
@@ -401,8 +461,9 @@ __global__ void __launch_bounds__(kMmThreads)
             const int t = nt * 8 + 2 * tig + (e & 1);
             if (t >= M) continue;
             const int row = (rb0 + r) * 16 + gid + ((e & 2) ? 8 : 0);
-            // acc carries the factor 2^-24 of the operand encoding
-            const float v = acc[r][nt][e] * (16777216.0f * __ldg(a_s + t));
+            // acc carries the factor 2^-24 of the operand encoding (and, per token, s_a: the
+            // per-32 mode has folded its scales into the group terms)
+            const float v = acc[r][nt][e] * (P32 ? 16777216.0f : 16777216.0f * __ldg(a_s + t));
             float* dst = y + (size_t)t * ldy + row;
             if (epi == EPI_ADD)
               *dst = *dst + v;
@@ -416,13 +477,19 @@ __global__ void __launch_bounds__(kMmThreads)
 }
 
 cudaError_t mm_configure() {
-  cudaError_t e = cudaFuncSetAttribute(k_mm<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmSmem);
+  cudaError_t e = cudaFuncSetAttribute(k_mm<1, kModeNormal>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mm_smem<1, kModeNormal>());
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_mm<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmSmem);
+  e = cudaFuncSetAttribute(k_mm<2, kModeNormal>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mm_smem<2, kModeNormal>());
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_mm<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmSmem);
+  e = cudaFuncSetAttribute(k_mm<4, kModeNormal>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mm_smem<4, kModeNormal>());
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_mm<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmSmem);
+  e = cudaFuncSetAttribute(k_mm<1, kModeFault>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mm_smem<1, kModeNormal>());
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_mm<2, kModeFault>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mm_smem<2, kModeNormal>());
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_mm<1, kModePer32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mm_smem<1, kModePer32>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_mm<2, kModePer32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mm_smem<2, kModePer32>());
 }
 
 cudaError_t mm_run(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, const uint8_t* act, const float* a_s,
@@ -436,13 +503,37 @@ cudaError_t mm_run(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, 
   const uint8_t* w8 = reinterpret_cast<const uint8_t*>(wt);
   const uint8_t* s8 = reinterpret_cast<const uint8_t*>(st);
   if (act_tiles(M) == 1)
-    return launch_pdl(k_mm<1, false>, grid, block, kMmSmem, stream, w8, s8, act, a_s, M, p.N, ldy, p.KC, p.cps, p.S,
-                      y, epi, part, tickets, err, stop);
-  return launch_pdl(k_mm<2, false>, grid, block, kMmSmem, stream, w8, s8, act, a_s, M, p.N, ldy, p.KC, p.cps, p.S, y,
-                    epi, part, tickets, err, stop);
+    return launch_pdl(k_mm<1, kModeNormal>, grid, block, mm_smem<1, kModeNormal>(), stream, w8, s8, act, a_s, M, p.N, ldy, p.KC, p.cps,
+                      p.S, y, epi, part, tickets, err, stop);
+  if (act_tiles(M) == 2)
+    return launch_pdl(k_mm<2, kModeNormal>, grid, block, mm_smem<2, kModeNormal>(), stream, w8, s8, act, a_s, M, p.N, ldy, p.KC, p.cps,
+                      p.S, y, epi, part, tickets, err, stop);
+  // 17..32 tokens (prefill buckets): split-K partials only (the in-kernel fold of the ticket path
+  // holds 16 token rows)
+  if (epi != EPI_PARTIAL) return cudaErrorInvalidValue;
+  return launch_pdl(k_mm<4, kModeNormal>, grid, block, mm_smem<4, kModeNormal>(), stream, w8, s8, act, a_s, M, p.N, ldy, p.KC, p.cps,
+                    p.S, y, epi, part, tickets, err, stop);
 }
 
 namespace {
+// The per-32 variant (EPI_STORE): activation records with per-group scales (act_prep_run with s32).
+cudaError_t mm_run_per32(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, const uint8_t* act, int M,
+                         float* y, float* part, unsigned* tickets, unsigned* err, cudaStream_t stream) {
+  static cudaError_t configured = mm_configure();
+  if (configured != cudaSuccess) return configured;
+  const long long units = (long long)p.n_rg * p.S;
+  dim3 grid((unsigned)(units < kPersistentCtas ? units : kPersistentCtas));
+  const uint8_t* w8 = reinterpret_cast<const uint8_t*>(wt);
+  const uint8_t* s8 = reinterpret_cast<const uint8_t*>(st);
+  const unsigned* no_stop = nullptr;
+  const float* no_scale = nullptr;
+  if (act_tiles(M) == 1)
+    return launch_pdl(k_mm<1, kModePer32>, grid, dim3(kMmThreads), mm_smem<1, kModePer32>(), stream, w8, s8, act,
+                      no_scale, M, p.N, p.N, p.KC, p.cps, p.S, y, (int)EPI_STORE, part, tickets, err, no_stop);
+  return launch_pdl(k_mm<2, kModePer32>, grid, dim3(kMmThreads), mm_smem<2, kModePer32>(), stream, w8, s8, act,
+                    no_scale, M, p.N, p.N, p.KC, p.cps, p.S, y, (int)EPI_STORE, part, tickets, err, no_stop);
+}
+
 // The test-only FAULT variant with the launch of mm_run (EPI_STORE).
 cudaError_t mm_run_fault(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, const uint8_t* act,
                          const float* a_s, int M, float* y, float* part, unsigned* tickets, unsigned* err,
@@ -455,21 +546,24 @@ cudaError_t mm_run_fault(const MatmulPlan& p, const uint32_t* wt, const uint16_t
   const uint8_t* s8 = reinterpret_cast<const uint8_t*>(st);
   const unsigned* no_stop = nullptr;
   if (act_tiles(M) == 1)
-    return launch_pdl(k_mm<1, true>, grid, dim3(kMmThreads), kMmSmem, stream, w8, s8, act, a_s, M, p.N, p.N, p.KC,
+    return launch_pdl(k_mm<1, kModeFault>, grid, dim3(kMmThreads), mm_smem<1, kModeNormal>(), stream, w8, s8, act, a_s, M, p.N, p.N, p.KC,
                       p.cps, p.S, y, (int)EPI_STORE, part, tickets, err, no_stop);
-  return launch_pdl(k_mm<2, true>, grid, dim3(kMmThreads), kMmSmem, stream, w8, s8, act, a_s, M, p.N, p.N, p.KC,
+  return launch_pdl(k_mm<2, kModeFault>, grid, dim3(kMmThreads), mm_smem<2, kModeNormal>(), stream, w8, s8, act, a_s, M, p.N, p.N, p.KC,
                     p.cps, p.S, y, (int)EPI_STORE, part, tickets, err, no_stop);
 }
 }  // namespace
 
 // One warp per (chunk, group, 8-token tile): lane (gid, tig) builds its f16 fragment word
 // of token 8*nt + gid and the group sums that seed the accumulators.
+// s32 (optional): per-32 activation scales [M][K/32], written after the corrections of each
+// chunk's record as [group 0..1][nt][tig] float2 {s(t0), s(t0+1)}, t0 = 8nt + 2tig (records of
+// 1216 bytes per tile).
 __global__ void k_act_prep(const int8_t* __restrict__ a_q, int M, int K, int lda, uint8_t* __restrict__ act,
-                           unsigned* __restrict__ tickets, int n_tickets) {
+                           unsigned* __restrict__ tickets, int n_tickets, const float* __restrict__ s32) {
   griddep_enter();
   const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
   for (int i = gtid; i < n_tickets; i += gridDim.x * blockDim.x) tickets[i] = 0u;
-  const int NT = act_tiles(M), rec = act_rec_bytes(NT);
+  const int NT = act_tiles(M), rec = NT * (s32 != nullptr ? 1216 : 1152);
   const int KC = chunks_of(K), G = K / 32;
   const int wid = gtid >> 5;  // (c, gg, nt)
   if (wid >= KC * 2 * NT) return;
@@ -506,14 +600,20 @@ __global__ void k_act_prep(const int8_t* __restrict__ a_q, int M, int K, int lda
     cq[0] = cv;
     cq[2] = cv;
   }
+  if (s32 != nullptr && gid == 0) {
+    const int t0 = nt * 8 + 2 * tig;
+    const float v0 = (t0 < M && g < G) ? s32[(size_t)t0 * G + g] : 0.0f;
+    const float v1 = (t0 + 1 < M && g < G) ? s32[(size_t)(t0 + 1) * G + g] : 0.0f;
+    reinterpret_cast<float2*>(rc + NT * 1152 + (gg * NT + nt) * 32)[tig] = make_float2(v0, v1);
+  }
 }
 
 cudaError_t act_prep_run(const int8_t* a_q, int M, int K, int lda, uint8_t* act, unsigned* tickets, int n_tickets,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, const float* s32) {
   const int warps = chunks_of(K) * 2 * act_tiles(M);
   const int threads = 128;
   const int blocks = (warps * 32 + threads - 1) / threads;
-  return launch_pdl(k_act_prep, dim3(blocks), dim3(threads), 0, stream, a_q, M, K, lda, act, tickets, n_tickets);
+  return launch_pdl(k_act_prep, dim3(blocks), dim3(threads), 0, stream, a_q, M, K, lda, act, tickets, n_tickets, s32);
 }
 
 }  // namespace w4a8
@@ -528,7 +628,7 @@ inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 MatmulWorkspace ws_layout(const MatmulPlan& p) {
   MatmulWorkspace w;
   w.off_act = 0;
-  w.off_part = align256(w.off_act + act_bytes(p.K));
+  w.off_part = align256(w.off_act + (size_t)chunks_of(p.K) * 2 * 1216);  // records of either activation mode
   w.off_tickets = align256(w.off_part + p.part_floats * 4);
   w.off_err = align256(w.off_tickets + (size_t)p.n_rg * 4);
   w.total = w.off_err + 256;
@@ -566,6 +666,46 @@ W4A8_API w4a8_status w4a8_matmul(const int8_t* a_q, const float* a_s, int M, int
   cudaStream_t st = as_stream(stream);
   W4A8_CUDA_TRY(act_prep_run(a_q, M, K, K, act, tickets, p.n_rg, st));
   W4A8_CUDA_TRY(mm_run(p, w_t, s_t, act, a_s, M, y, N, EPI_STORE, part, tickets, err, nullptr, st));
+  return W4A8_OK;
+}
+
+W4A8_API w4a8_status w4a8_matmul_per32(const int8_t* a_q, const float* a_s, int M, int K, const uint32_t* w_t,
+                                       const uint16_t* s_t, int N, float* y, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  if (!a_q || !a_s || !w_t || !s_t || !y || !workspace || M <= 0 || K <= 0 || N <= 0) return W4A8_ERR_ARG;
+  if (M > 16 || K % 32 || N % 16) return W4A8_ERR_SHAPE;
+  if (!aligned(w_t, 16) || !aligned(s_t, 16) || !aligned(workspace, 256) || !aligned(a_q, 4) || !aligned(a_s, 4))
+    return W4A8_ERR_ARG;
+  const MatmulPlan p = mm_plan(K, N);
+  const MatmulWorkspace w = ws_layout(p);
+  if (workspace_bytes < w.total) return W4A8_ERR_CAPACITY;
+  char* base = static_cast<char*>(workspace);
+  cudaStream_t st = as_stream(stream);
+  uint8_t* act = reinterpret_cast<uint8_t*>(base + w.off_act);
+  unsigned* tickets = reinterpret_cast<unsigned*>(base + w.off_tickets);
+  W4A8_CUDA_TRY(act_prep_run(a_q, M, K, K, act, tickets, p.n_rg, st, a_s));
+  W4A8_CUDA_TRY(mm_run_per32(p, w_t, s_t, act, M, y, reinterpret_cast<float*>(base + w.off_part), tickets,
+                             reinterpret_cast<unsigned*>(base + w.off_err), st));
+  return W4A8_OK;
+}
+
+W4A8_API w4a8_status w4a8_matmul_nondet(const int8_t* a_q, const float* a_s, int M, int K, const uint32_t* w_t,
+                                        const uint16_t* s_t, int N, float* y, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  if (!a_q || !a_s || !w_t || !s_t || !y || !workspace || M <= 0 || K <= 0 || N <= 0) return W4A8_ERR_ARG;
+  if (M > 16 || K % 32 || N % 16) return W4A8_ERR_SHAPE;
+  if (!aligned(w_t, 16) || !aligned(s_t, 16) || !aligned(workspace, 256) || !aligned(a_q, 4) || !aligned(a_s, 4))
+    return W4A8_ERR_ARG;
+  const MatmulPlan p = mm_plan(K, N);
+  const MatmulWorkspace w = ws_layout(p);
+  if (workspace_bytes < w.total) return W4A8_ERR_CAPACITY;
+  char* base = static_cast<char*>(workspace);
+  cudaStream_t st = as_stream(stream);
+  uint8_t* act = reinterpret_cast<uint8_t*>(base + w.off_act);
+  W4A8_CUDA_TRY(cudaMemsetAsync(y, 0, (size_t)M * N * sizeof(float), st));
+  W4A8_CUDA_TRY(act_prep_run(a_q, M, K, K, act, nullptr, 0, st));
+  W4A8_CUDA_TRY(mm_run(p, w_t, s_t, act, a_s, M, y, N, EPI_ATOMIC, nullptr, nullptr,
+                       reinterpret_cast<unsigned*>(base + w.off_err), nullptr, st));
   return W4A8_OK;
 }
 

@@ -22,15 +22,20 @@ constexpr int kRowsPerCta = 16 * kWarpsPerCta * kRowBlocksPerWarp;  // 256
 
 MatmulPlan mm_plan(int K, int N);
 
-// floats of the EPI_PARTIAL output of a plan: [S][16 tokens][N]
-inline size_t mm_partial_floats(const MatmulPlan& p) { return (size_t)p.S * 16 * p.N; }
+// Token rows of the EPI_PARTIAL layout (the widest token count a decoder pass uses: a prefill
+// bucket of 32 prompt tokens).
+constexpr int kPartTokens = 32;
+// floats of the EPI_PARTIAL output of a plan: [S][kPartTokens][N]
+inline size_t mm_partial_floats(const MatmulPlan& p) { return (size_t)p.S * kPartTokens * p.N; }
 
 // Output handling after the fixed-order reduction: y = fold * s_a[t], then
 enum MatmulEpilogue : int {
   EPI_STORE = 0,    // y[t][n] = value
   EPI_ADD = 1,      // y[t][n] += value (residual stream)
-  EPI_PARTIAL = 2,  // part[(s * 16 + t) * N + n] = slice s's unscaled sum, t < M; y unused.  The
+  EPI_PARTIAL = 2,  // part[(s * kPartTokens + t) * N + n] = slice s's unscaled sum, t < M; y unused.  The
                     // consumer folds the slices with mm_fold4 / mm_fold2 (no tickets, no fence)
+  EPI_ATOMIC = 3,   // y[t][n] += slice value * s_a[t] with a float atomic (y zeroed before): the slices
+                    // combine in arrival order -- not deterministic (the fast variant)
 };
 
 // Launches the matmul kernel on prepared activation records.  part/tickets: split-K
@@ -58,7 +63,7 @@ __device__ __forceinline__ float4 mm_fold4(const float* part, int S, int N, int 
     float4 v[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q)
-      if (sb + q < S) v[q] = *reinterpret_cast<const float4*>(part + ((size_t)(sb + q) * 16 + t) * N + n);
+      if (sb + q < S) v[q] = *reinterpret_cast<const float4*>(part + ((size_t)(sb + q) * kPartTokens + t) * N + n);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       if (sb + q >= S) break;
@@ -80,8 +85,8 @@ __device__ __forceinline__ float2 mm_fold2(const float* part, int S, int N, int 
 #pragma unroll
     for (int q = 0; q < 16; ++q)
       if (sb + q < S) {
-        v0[q] = part[((size_t)(sb + q) * 16 + t) * N + n0];
-        v1[q] = part[((size_t)(sb + q) * 16 + t) * N + n1];
+        v0[q] = part[((size_t)(sb + q) * kPartTokens + t) * N + n0];
+        v1[q] = part[((size_t)(sb + q) * kPartTokens + t) * N + n1];
       }
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
@@ -101,7 +106,7 @@ cudaError_t repack_run(const uint32_t* w_p2, const uint16_t* s_p2, int N, int K,
 // Launches the record builder for int8 activations a_q[M][K] (row stride lda) and zeroes
 // n_tickets counters.
 cudaError_t act_prep_run(const int8_t* a_q, int M, int K, int lda, uint8_t* act, unsigned* tickets, int n_tickets,
-                         cudaStream_t stream);
+                         cudaStream_t stream, const float* s32 = nullptr);
 
 // Device helpers for fused producers of the activation records (layout.cuh), for M tokens
 // (NT = act_tiles(M) tiles).

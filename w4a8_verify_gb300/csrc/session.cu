@@ -60,6 +60,7 @@ struct Arena {
   } while (0)
 
 constexpr int kMaxWindow = 64;
+constexpr int kMaxMemory = 32768;  // session-memory entries (the pages' 32K-token budget)
 constexpr int kRecBytesFixed = 32;
 constexpr int kRecStepBytes = (int)sizeof(StepStats) + kMaxWidth * 4;
 }  // namespace
@@ -93,15 +94,16 @@ struct w4a8_session {
     int slot, W, N;
   };
   std::deque<Flight> q;
+  std::vector<int32_t> mem_host;           // host copy of the session memory
   int next_slot = 0;
   std::map<long long, cudaGraphExec_t> graphs;
   std::map<long long, int> graph_kernels;  // kernel nodes of each window graph
-  cudaGraphExec_t chain_graph = nullptr;   // one prefill chain of kMaxWidth prompt tokens
+  cudaGraphExec_t bucket_graph = nullptr;  // one prefill bucket of kMaxBucket prompt tokens
   long long host_syncs = 0;
   long long kernels = 0;                   // kernels launched by window graphs
   ~w4a8_session() {
     for (auto& kv : graphs) cudaGraphExecDestroy(kv.second);
-    if (chain_graph) cudaGraphExecDestroy(chain_graph);
+    if (bucket_graph) cudaGraphExecDestroy(bucket_graph);
     for (int i = 0; i < 2; ++i)
       if (ev[i]) cudaEventDestroy(ev[i]);
     if (cap) cudaStreamDestroy(cap);
@@ -148,12 +150,16 @@ size_t trace_bytes(const ModelDims& d, int N) {
 
 // trace: optional device buffer of trace_bytes(d, N) bytes receiving the int8 codes of every
 // quantisation point (tests and tools; not used by the decoding loop).
-cudaError_t forward(w4a8_session* s, int N, bool head, float* logits_out, cudaStream_t st, int8_t* trace = nullptr) {
+// chain: a prefill bucket of N = kMaxBucket context tokens from committed_len (the current tree
+// must be the chain of kMaxWidth nodes, which the attention takes for each half of the bucket);
+// otherwise the current tree's first N nodes.
+cudaError_t forward(w4a8_session* s, int N, bool head, float* logits_out, cudaStream_t st, int8_t* trace = nullptr,
+                    bool chain = false) {
   const DecoderBufs& b = s->b;
   w4a8_model* m = s->m;
   const ModelDims& d = m->d;
   unsigned* flags = &b.ctl->flags;
-  TRYC(launch_embed(b, d, N, m->emb_w, m->emb_s, st));
+  TRYC(launch_embed(b, d, N, chain, m->emb_w, m->emb_s, st));
   // The layer projections leave per-slice partial sums (EPI_PARTIAL) that the next kernel
   // folds: RoPE/KV, the residual update before RMSNorm, SwiGLU.
   const float* res = nullptr;
@@ -170,7 +176,7 @@ cudaError_t forward(w4a8_session* s, int N, bool head, float* logits_out, cudaSt
     TRYC(trace_codes(d.H));
     TRYC(mm_run(m->p_qkv, m->qkv_w[l], m->qkv_s[l], b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets,
                 flags, flags, st));
-    TRYC(launch_rope_kv(b, d, N, l, m->p_qkv.S, st));
+    TRYC(launch_rope_kv(b, d, N, chain, l, m->p_qkv.S, st));
     TRYC(launch_attention(b, d, N, l, st));
     TRYC(trace_codes(d.Hq * d.D));
     TRYC(mm_run(m->p_o, m->o_w[l], m->o_s[l], b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets, flags,
@@ -309,7 +315,9 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
   if (desc->kv_cap < kMaxWidth + 1 || desc->ctx_cap < kMaxCont + 2 || desc->max_window < 1 ||
       desc->max_window > kMaxWindow)
     return W4A8_ERR_ARG;
-  if (desc->ctx_cap > 200 * 1024) return W4A8_ERR_CAPACITY;
+  if (desc->mem_cap < 0 || desc->mem_cap > kMaxMemory) return W4A8_ERR_ARG;
+  // the drafter keeps one byte per scanned position (context and memory) in shared memory
+  if (desc->ctx_cap > 200 * 1024 || desc->ctx_cap + desc->mem_cap > 220 * 1024) return W4A8_ERR_CAPACITY;
   const ModelDims& d = m->d;
   w4a8_session* s = new (std::nothrow) w4a8_session();
   if (!s) return W4A8_ERR_NOMEM;
@@ -321,6 +329,7 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
   b.n_chunks = (desc->kv_cap + kAttnChunk - 1) / kAttnChunk;
   b.max_window = desc->max_window;
   b.eos_id = desc->eos_id;
+  b.mem_cap = desc->mem_cap;
   const int Kmax = std::max(std::max(d.H, d.F), d.Hq * d.D);
   // per-slice outputs of the projections (EPI_PARTIAL)
   size_t part = std::max({mm_partial_floats(m->p_lm), mm_partial_floats(m->p_qkv), mm_partial_floats(m->p_o),
@@ -328,21 +337,24 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
   int tick = std::max({m->p_qkv.n_rg, m->p_o.n_rg, m->p_gu.n_rg, m->p_dn.n_rg, m->p_lm.n_rg});
   const size_t kv = (size_t)d.n_layers * d.Hkv * desc->kv_cap * d.D * sizeof(float);
   Arena& A = s->arena;
+  constexpr int kChains = kMaxBucket / kMaxWidth;  // attention chains of a prefill bucket
+  const int QD = d.Hq * d.D;
   bool ok = A.dalloc(&b.ctl, sizeof(SpecCtl)) && A.dalloc(&b.tree, sizeof(TreeState)) &&
             A.dalloc(&b.rec, sizeof(AcceptRec)) && A.dalloc(&b.ctx, (size_t)desc->ctx_cap * 4) &&
-            A.dalloc(&b.pred, kMaxWidth * 4) && A.dalloc(&b.x, (size_t)kMaxWidth * d.H * 4) &&
-            A.dalloc(&b.qkv, (size_t)kMaxWidth * m->qkv_rows * 4) &&
-            A.dalloc(&b.qrot, (size_t)kMaxWidth * d.Hq * d.D * 4) && A.dalloc(&b.gu, (size_t)kMaxWidth * 2 * d.F * 4) &&
+            A.dalloc(&b.pred, kMaxWidth * 4) && A.dalloc(&b.x, (size_t)kMaxBucket * d.H * 4) &&
+            A.dalloc(&b.qkv, (size_t)kMaxBucket * std::max(m->qkv_rows, QD) * 4) &&
+            A.dalloc(&b.qrot, (size_t)kMaxBucket * QD * 4) && A.dalloc(&b.gu, (size_t)kMaxBucket * 2 * d.F * 4) &&
             A.dalloc(&b.logits, (size_t)kMaxWidth * d.V * 4) &&
-            A.dalloc(&b.o_part, (size_t)b.n_chunks * kMaxWidth * d.Hq * d.D * 4) &&
-            A.dalloc(&b.ml_part, (size_t)b.n_chunks * kMaxWidth * d.Hq * 8) &&
-            A.dalloc(&b.act, act_bytes(Kmax)) &&
-            A.dalloc(&b.a_s, kMaxWidth * 4) && A.dalloc(&b.mm_part, part * 4) && A.dalloc(&b.tickets, (size_t)tick * 4) &&
+            A.dalloc(&b.o_part, (size_t)kChains * b.n_chunks * kMaxWidth * QD * 4) &&
+            A.dalloc(&b.ml_part, (size_t)kChains * b.n_chunks * kMaxWidth * d.Hq * 8) &&
+            A.dalloc(&b.act, act_bytes_nt(Kmax, act_tiles(kMaxBucket))) &&
+            A.dalloc(&b.a_s, kMaxBucket * 4) && A.dalloc(&b.mm_part, part * 4) && A.dalloc(&b.tickets, (size_t)tick * 4) &&
             A.dalloc(&b.kcache, kv) && A.dalloc(&b.vcache, kv) &&
             A.dalloc(&b.rope, (size_t)desc->kv_cap * (d.D / 2) * sizeof(float2)) &&
-            A.dalloc(&b.qpart, (size_t)kMaxWidth * (std::max({d.H, d.F, d.Hq * d.D}) / 512 + d.Hq + 2) * sizeof(float2)) &&
+            A.dalloc(&b.qpart, (size_t)kMaxBucket * (std::max({d.H, d.F, QD}) / 512 + d.Hq + 2) * sizeof(float2)) &&
             A.dalloc(&b.argmax_part, (size_t)kMaxWidth * ((d.V + 8191) / 8192) * sizeof(float2)) &&
-            A.dalloc(&b.argmax_tickets, kMaxWidth * 4) && A.dalloc(&b.attn_tickets, (size_t)d.Hkv * 4) &&
+            A.dalloc(&b.argmax_tickets, kMaxWidth * 4) && A.dalloc(&b.attn_tickets, (size_t)kChains * d.Hkv * 4) &&
+            A.dalloc(&b.mem, (size_t)std::max(desc->mem_cap, 1) * 4) && A.dalloc(&b.mem_len, sizeof(int)) &&
             A.dalloc(&b.wstats, (size_t)desc->max_window * sizeof(StepStats)) &&
             A.dalloc(&b.wtok, (size_t)desc->max_window * kMaxWidth * 4) &&
             A.dalloc(&s->dev_rec, kRecBytesFixed + (size_t)desc->max_window * kRecStepBytes) &&
@@ -356,12 +368,13 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
   }
   // zero everything that is read before written (fragment padding groups, tickets, records)
   cudaError_t e = cudaSuccess;
-  e = e == cudaSuccess ? cudaMemset(b.act, 0, act_bytes(Kmax)) : e;
+  e = e == cudaSuccess ? cudaMemset(b.act, 0, act_bytes_nt(Kmax, act_tiles(kMaxBucket))) : e;
   e = e == cudaSuccess ? cudaMemset(b.tickets, 0, (size_t)tick * 4) : e;
   e = e == cudaSuccess ? cudaMemset(b.argmax_tickets, 0, kMaxWidth * 4) : e;
-  e = e == cudaSuccess ? cudaMemset(b.attn_tickets, 0, (size_t)d.Hkv * 4) : e;
+  e = e == cudaSuccess ? cudaMemset(b.attn_tickets, 0, (size_t)kChains * d.Hkv * 4) : e;
   e = e == cudaSuccess ? cudaMemset(b.ctl, 0, sizeof(SpecCtl)) : e;
   e = e == cudaSuccess ? cudaMemset(b.rec, 0, sizeof(AcceptRec)) : e;
+  e = e == cudaSuccess ? cudaMemset(b.mem_len, 0, sizeof(int)) : e;
   e = e == cudaSuccess ? cudaMemset(b.tree, 0, sizeof(TreeState)) : e;
   e = e == cudaSuccess ? cudaMemset(b.kcache, 0, kv) : e;
   e = e == cudaSuccess ? cudaMemset(b.vcache, 0, kv) : e;
@@ -379,7 +392,7 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
   e = e == cudaSuccess ? attn_configure(d, attn_smem_bytes(d.D, kMaxWidth * (d.Hq / d.Hkv))) : e;
   e = e == cudaSuccess ? attn_tensor_maps(b, d) : e;
   e = e == cudaSuccess ? mm_configure() : e;
-  e = e == cudaSuccess ? draft_configure(desc->ctx_cap) : e;
+  e = e == cudaSuccess ? draft_configure(desc->ctx_cap + desc->mem_cap) : e;
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     delete s;
@@ -394,6 +407,10 @@ W4A8_API void w4a8_session_destroy(w4a8_session* s) {
   delete s;
 }
 
+namespace {
+bool d_ok_for_buckets(const ModelDims& d) { return d.Hq / d.Hkv >= 2; }
+}  // namespace
+
 W4A8_API w4a8_status w4a8_prefill(w4a8_session* s, const int32_t* prompt, int n, int max_new, void* stream) {
   if (!s || !prompt || n < 1 || max_new < 0) return W4A8_ERR_ARG;
   if (!s->q.empty()) return W4A8_ERR_ARG;
@@ -403,31 +420,39 @@ W4A8_API w4a8_status w4a8_prefill(w4a8_session* s, const int32_t* prompt, int n,
   cudaStream_t st = as_stream(stream);
   W4A8_CUDA_TRY(cudaMemcpyAsync(b.ctx, prompt, (size_t)n * 4, cudaMemcpyDeviceToDevice, st));
   W4A8_CUDA_TRY(launch_pdl(k_init_ctl, dim3(1), dim3(32), 0, st, b.ctl, b.rec, (const int32_t*)b.ctx, n, max_new));
-  // Full chains replay one captured graph (the chain kernels read their position from the
-  // control word); the last, shorter chain is launched directly.
-  const int full = (n - 1) / kMaxWidth;
-  if (full > 0 && !s->chain_graph) {
+  // Integer prefill in wide buckets [P1 Small-Batch Verification Kernels: bucket of 32 tokens;
+  // Experiments: request latency]: full buckets of kMaxBucket prompt tokens replay one captured
+  // graph (the kernels read their position from the control word): the matmuls and the row-wise
+  // kernels take the whole bucket, the attention its two chains of kMaxWidth.  The rest runs as
+  // chains of up to kMaxWidth nodes through the verification kernels.  Every step of a token's
+  // forward is row-local with the same order, so the cache holds the bits of sequential steps.
+  // (models whose query heads do not share KV heads keep chains of kMaxWidth: their attention
+  // merges inside the chunk kernel, which takes one chain per launch)
+  const int buckets = d_ok_for_buckets(s->m->d) ? (n - 1) / kMaxBucket : 0;
+  if (buckets > 0 && !s->bucket_graph) {
     cudaGraph_t g = nullptr;
     W4A8_CUDA_TRY(cudaStreamBeginCapture(s->cap, cudaStreamCaptureModeThreadLocal));
     cudaError_t e = launch_chain_tree(b, 0, kMaxWidth, s->cap);
-    if (e == cudaSuccess) e = forward(s, kMaxWidth, false, nullptr, s->cap);
-    if (e == cudaSuccess) e = launch_commit_chain(b, kMaxWidth, s->cap);
+    if (e == cudaSuccess) e = forward(s, kMaxBucket, false, nullptr, s->cap, nullptr, true);
+    if (e == cudaSuccess) e = launch_commit_chain(b, kMaxBucket, s->cap);
     const cudaError_t e2 = cudaStreamEndCapture(s->cap, &g);
     if (e == cudaSuccess) e = e2;
-    if (e == cudaSuccess) e = cudaGraphInstantiate(&s->chain_graph, g, 0);
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&s->bucket_graph, g, 0);
     if (g) cudaGraphDestroy(g);
     if (e != cudaSuccess) {
-      s->chain_graph = nullptr;
+      s->bucket_graph = nullptr;
       (void)cudaGetLastError();
       return W4A8_ERR_CUDA;
     }
   }
-  for (int c = 0; c < full; ++c) W4A8_CUDA_TRY(cudaGraphLaunch(s->chain_graph, st));
-  const int rest = n - 1 - full * kMaxWidth;
-  if (rest > 0) {
-    W4A8_CUDA_TRY(launch_chain_tree(b, full * kMaxWidth, rest, st));
-    W4A8_CUDA_TRY(forward(s, rest, false, nullptr, st));
-    W4A8_CUDA_TRY(launch_commit_chain(b, rest, st));
+  for (int c = 0; c < buckets; ++c) W4A8_CUDA_TRY(cudaGraphLaunch(s->bucket_graph, st));
+  int done = buckets * kMaxBucket;
+  while (done < n - 1) {
+    const int len = std::min(kMaxWidth, n - 1 - done);
+    W4A8_CUDA_TRY(launch_chain_tree(b, done, len, st));
+    W4A8_CUDA_TRY(forward(s, len, false, nullptr, st));
+    W4A8_CUDA_TRY(launch_commit_chain(b, len, st));
+    done += len;
   }
   W4A8_CUDA_TRY(launch_draft(b, 1, st));
   return W4A8_OK;
@@ -884,6 +909,48 @@ W4A8_API w4a8_status w4a8_session_get_context(w4a8_session* s, int32_t* out, int
   *n = (int)c.ctx_len;
   const int k = std::min(cap, (int)c.ctx_len);
   if (k > 0) return sync_read(s, out, s->b.ctx, (size_t)k * 4);
+  return W4A8_OK;
+}
+
+W4A8_API w4a8_status w4a8_session_memory_append(w4a8_session* s, const int32_t* tokens, int n) {
+  if (!s || (!tokens && n > 0) || n < 0) return W4A8_ERR_ARG;
+  if (!s->q.empty()) return W4A8_ERR_ARG;
+  const int cap = s->b.mem_cap;
+  if (cap < 2) return W4A8_ERR_CAPACITY;
+  for (int i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= s->m->d.V) return W4A8_ERR_ARG;
+  // an output longer than the memory keeps its last cap - 1 tokens; whole outputs are dropped
+  // from the oldest until the new one fits
+  const int keep = std::min(n, cap - 1);
+  std::vector<int32_t>& mh = s->mem_host;
+  while (!mh.empty() && (int)mh.size() + keep + 1 > cap) {
+    size_t nxt = 1;
+    while (nxt < mh.size() && mh[nxt] != -1) ++nxt;
+    mh.erase(mh.begin(), mh.begin() + (long)nxt);
+  }
+  mh.push_back(-1);
+  mh.insert(mh.end(), tokens + (n - keep), tokens + n);
+  const int len = (int)mh.size();
+  W4A8_CUDA_TRY(cudaDeviceSynchronize());
+  W4A8_CUDA_TRY(cudaMemcpy(s->b.mem, mh.data(), (size_t)len * 4, cudaMemcpyHostToDevice));
+  W4A8_CUDA_TRY(cudaMemcpy(s->b.mem_len, &len, sizeof(int), cudaMemcpyHostToDevice));
+  return W4A8_OK;
+}
+
+W4A8_API w4a8_status w4a8_session_memory_clear(w4a8_session* s) {
+  if (!s || !s->q.empty()) return W4A8_ERR_ARG;
+  s->mem_host.clear();
+  const int zero = 0;
+  W4A8_CUDA_TRY(cudaDeviceSynchronize());
+  W4A8_CUDA_TRY(cudaMemcpy(s->b.mem_len, &zero, sizeof(int), cudaMemcpyHostToDevice));
+  return W4A8_OK;
+}
+
+W4A8_API w4a8_status w4a8_session_memory_get(const w4a8_session* s, int32_t* out, int cap, int* n) {
+  if (!s || !n || cap < 0 || (!out && cap > 0)) return W4A8_ERR_ARG;
+  *n = (int)s->mem_host.size();
+  const int k = std::min(cap, *n);
+  if (k > 0) std::memcpy(out, s->mem_host.data(), (size_t)k * 4);
   return W4A8_OK;
 }
 

@@ -148,12 +148,16 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
 
 // One CTA of kDraftThreads.  Writes the full-width tree (kMaxWidth nodes) in best-first order:
 // the first N nodes of it are the tree of width N.
+// The scan covers the session memory (mem[0 .. *mem_len), earlier outputs each preceded by the
+// separator -1, which equals no token) and then the context: scan position v < m is memory
+// entry v, v >= m context position v - m.  A memory match stops at a separator, a memory
+// continuation ends before the next one, and a higher scan position is the more recent.
 __global__ void __launch_bounds__(kDraftThreads)
-    k_draft(SpecCtl* ctl, const AcceptRec* __restrict__ rec, const int32_t* __restrict__ ctx, TreeState* tree,
-            int force) {
+    k_draft(SpecCtl* ctl, const AcceptRec* __restrict__ rec, const int32_t* __restrict__ ctx,
+            const int32_t* __restrict__ mem, const int* __restrict__ mem_len, TreeState* tree, int force) {
   griddep_enter();
   if (!force && (!rec->valid || (ctl->flags & FLAG_ERR_MASK))) return;
-  extern __shared__ uint8_t s_ell[];  // match length per context position
+  extern __shared__ uint8_t s_ell[];  // match length per scan position
   __shared__ int s_suf[kMaxCont];
   __shared__ int s_warp[kDraftThreads / 32];
   __shared__ int s_cand[kCand];
@@ -162,22 +166,29 @@ __global__ void __launch_bounds__(kDraftThreads)
   __shared__ int s_new[kCand][kMaxCont], s_score[kCand][kMaxCont], s_rep[kCand][kMaxCont], s_rank[kCand][kMaxCont];
   __shared__ int s_nnew;
   const int n = (int)ctl->ctx_len;
+  const int m = mem_len != nullptr ? *mem_len : 0;
   const int tid = threadIdx.x;
-  if (tid < kMaxCont) s_suf[tid] = (n - 1 - tid >= 0) ? ctx[n - 1 - tid] : -1;
+  // past the context's start the suffix holds -2, which neither a token nor a separator equals
+  if (tid < kMaxCont) s_suf[tid] = (n - 1 - tid >= 0) ? ctx[n - 1 - tid] : -2;
   if (tid < kCand) s_cand[tid] = -1;
   __syncthreads();
-  // 1) match lengths over positions [0, n-2], each thread a descending segment
-  const int P = n - 1;
+  // 1) match lengths over the scan positions [0, m + n - 2], each thread a descending segment
+  const int P = m + n - 1;
   const int seg = (P + kDraftThreads - 1) / kDraftThreads;
   const int hi = P - 1 - tid * seg;  // highest position of this thread's segment
   const int lo = max(0, P - (tid + 1) * seg);
   int cnt[kMaxCont + 1];
 #pragma unroll
   for (int l = 0; l <= kMaxCont; ++l) cnt[l] = 0;
-  for (int p = hi; p >= lo; --p) {
+  for (int v = hi; v >= lo; --v) {
     int l = 0;
-    while (l < kMaxCont && p - l >= 0 && ctx[p - l] == s_suf[l]) ++l;
-    s_ell[p] = (uint8_t)l;
+    if (v >= m) {
+      const int p = v - m;
+      while (l < kMaxCont && p - l >= 0 && ctx[p - l] == s_suf[l]) ++l;
+    } else {
+      while (l < kMaxCont && v - l >= 0 && mem[v - l] == s_suf[l]) ++l;
+    }
+    s_ell[v] = (uint8_t)l;
     cnt[l] += 1;
   }
   // 2) rank of every matched position inside its class (descending position)
@@ -205,11 +216,22 @@ __global__ void __launch_bounds__(kDraftThreads)
   __syncthreads();
   // 3) continuations of the candidates
   if (tid < kCand) {
-    const int p = s_cand[tid];
-    const int len = (tid < n_cand && p >= 0) ? min(kMaxCont, n - 1 - p) : 0;
+    const int v = s_cand[tid];
+    const bool on = tid < n_cand && v >= 0;
+    int len = 0;
+    if (on && v >= m) {
+      const int p = v - m;
+      len = min(kMaxCont, n - 1 - p);
+      for (int k = 0; k < kMaxCont; ++k) s_cont[tid][k] = k < len ? ctx[p + 1 + k] : -1;
+    } else {
+      for (int k = 0; k < kMaxCont; ++k) {
+        const int t = (on && v + 1 + k < m && len == k) ? mem[v + 1 + k] : -1;
+        if (t >= 0) ++len;
+        s_cont[tid][k] = k < len ? t : -1;
+      }
+    }
     s_len[tid] = len;
-    s_w[tid] = (tid < n_cand && p >= 0) ? (int)s_ell[p] : 0;
-    for (int k = 0; k < kMaxCont; ++k) s_cont[tid][k] = k < len ? ctx[p + 1 + k] : -1;
+    s_w[tid] = on ? (int)s_ell[v] : 0;
   }
   __syncthreads();
   // 4) trie nodes = distinct prefixes; thread (i, L) for i < 16, L = 1..8
@@ -309,12 +331,18 @@ cudaError_t launch_compact(const DecoderBufs& b, const ModelDims& m, cudaStream_
 }
 
 cudaError_t launch_draft(const DecoderBufs& b, int force, cudaStream_t st) {
-  return launch_pdl(k_draft, dim3(1), dim3(kDraftThreads), (size_t)b.ctx_cap, st, b.ctl, (const AcceptRec*)b.rec,
-                    (const int32_t*)b.ctx, b.tree, force);
+  return launch_pdl(k_draft, dim3(1), dim3(kDraftThreads), (size_t)b.ctx_cap + b.mem_cap, st, b.ctl,
+                    (const AcceptRec*)b.rec, (const int32_t*)b.ctx, (const int32_t*)b.mem, (const int*)b.mem_len,
+                    b.tree, force);
 }
 
-cudaError_t draft_configure(int ctx_cap) {
-  return cudaFuncSetAttribute(k_draft, cudaFuncAttributeMaxDynamicSharedMemorySize, ctx_cap);
+cudaError_t draft_configure(int scan_cap) {
+  // the attribute is per kernel, shared by every session: only ever raised
+  static int configured = 0;
+  if (scan_cap <= configured) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(k_draft, cudaFuncAttributeMaxDynamicSharedMemorySize, scan_cap);
+  if (e == cudaSuccess) configured = scan_cap;
+  return e;
 }
 
 cudaError_t launch_chain_tree(const DecoderBufs& b, int start, int len, cudaStream_t st) {
