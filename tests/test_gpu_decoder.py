@@ -510,3 +510,52 @@ def test_cancel_by_terminate_flag(tiny):
     n = s.ctl().n_generated
     s.spec_step(4)
     assert s.ctl().n_generated == n
+
+
+# ------------------------------------------------------------------------- edge sizes
+
+@pytest.mark.parametrize("n", [2, 17, 32, 33, 34, 64, 65, 66, 97])
+def test_prefill_bucket_edges_equal_sequential_kv(tiny, n):
+    """Prompts whose length puts the prefill on either side of the 32-token bucket edges (and
+    the rest on the chain edges) leave the bits of sequential single-token steps."""
+    rng = np.random.default_rng(n)
+    prompt = rng.integers(0, SHAPE.vocab, size=n).tolist()
+    s = _session(tiny, kv_cap=n + 24, ctx_cap=n + 24)      # the cache exactly as large as prefill + 8 + 16 needs
+    s.prefill(_dev(prompt), max_new=8)
+    _, seq = _forced_sequential_logits(tiny, prompt[:-1]) if n > 1 else (None, None)
+    L = n - 1
+    for layer in range(SHAPE.n_layers):
+        k1, v1, k2, v2 = (torch.empty((SHAPE.n_kv_heads, L, SHAPE.head_dim), dtype=torch.float32, device="cuda")
+                          for _ in range(4))
+        s.copy_kv(layer, 0, L, k1, v1)
+        seq.copy_kv(layer, 0, L, k2, v2)
+        torch.cuda.synchronize()
+        assert torch.equal(k1, k2) and torch.equal(v1, v2), (n, layer)
+    c = s.ctl()
+    assert c.committed_len == L and c.ctx_len == n
+
+
+def test_prefill_refuses_a_cache_one_slot_short(tiny):
+    prompt = list(tiny["prompt"])
+    s = _session(tiny, kv_cap=len(prompt) + 8 + 16 - 1, ctx_cap=512)
+    with pytest.raises(W.W4A8Error) as e:
+        s.prefill(_dev(prompt), max_new=8)
+    assert e.value.status == 4
+
+
+def test_draft_with_a_full_32k_memory_matches_oracle(tiny):
+    rng = np.random.default_rng(33)
+    motifs = rng.integers(0, 50, size=(6, 12))
+    seq = np.concatenate([motifs[i] for i in rng.integers(0, 6, size=4000)]).tolist()
+    segs = [seq[i:i + 700] for i in range(0, len(seq), 700)]            # > 32768 entries in total
+    ctx = seq[:300]
+    s = _session(tiny, kv_cap=600, ctx_cap=1024, mem_cap=32768)
+    for seg in segs:
+        s.memory_append(seg)
+    mem = OS.memory_array(segs, 32768)
+    assert s.memory() == mem and len(mem) > 32000
+    s.prefill(_dev(np.asarray(ctx, np.int32)), max_new=1)
+    tok, par, dep, n_valid, best = s.tree()
+    o_tok, o_par, o_nv, o_best = OS.draft(ctx, 16, memory=mem)
+    assert (n_valid, best) == (o_nv, o_best)
+    assert tok[:n_valid] == o_tok[:n_valid].tolist() and par[1:n_valid] == o_par[1:n_valid].tolist()

@@ -23,7 +23,7 @@
 namespace w4a8 {
 
 namespace {
-constexpr int kChunkBatch = 2;           // 64-input chunks per pipeline stage
+constexpr int kChunkBatch = 4;           // 64-input chunks per pipeline stage
 constexpr int kPersistentCtas = 304;     // fixed constant (2 x 152 SMs): part of the canonical schedule
 constexpr double kUnitFixedChunks = 1.0;  // modelled per-unit overhead, in chunk-streaming times
 }  // namespace
@@ -106,7 +106,7 @@ __device__ __forceinline__ void unpack_codes(uint32_t x, uint32_t (&r)[4]) {
 }
 
 constexpr int kRowBlocksPerCta = kWarpsPerCta * kRowBlocksPerWarp;   // 16
-static_assert(kChunkBatch == 2, "a stage holds one or two chunks");
+static_assert(kChunkBatch >= 1, "a stage holds whole chunks");
 static_assert(kRowBlocksPerCta == kGroupBlocks, "a CTA covers one row group of the tiled layout");
 // Shared-memory stage: weights [chunk][16 blocks][512 B], scales [chunk][16 blocks][64 B],
 // activation records [chunk][NT * 1152 B]; a row group with fewer blocks leaves a gap.
@@ -123,7 +123,7 @@ template <int MODE> constexpr int rec_tile_bytes() { return MODE == kModePer32 ?
 template <int NT, int MODE = kModeNormal> constexpr int stage_bytes() {
   return kStageA0 + kChunkBatch * (NT > 2 ? NT : 2) * rec_tile_bytes<MODE>();
 }
-constexpr int kStages = 4;
+constexpr int kStages = 2;
 constexpr int kMmThreads = 32 * (kWarpsPerCta + 1);                  // + one producer warp
 template <int NT, int MODE = kModeNormal> constexpr size_t mm_smem() {
   return (size_t)kStages * stage_bytes<NT, MODE>();
@@ -343,10 +343,11 @@ __global__ void __launch_bounds__(kMmThreads)
         const uint8_t* stage = smem + (size_t)stg * stage_bytes<NT, MODE>();
         // warps past the last row block of a short row group compute on the gap (results
         // are not stored)
-        if (c1 - (c0 + b * kChunkBatch) >= kChunkBatch)
+        const int ncs = min(kChunkBatch, c1 - (c0 + b * kChunkBatch));
+        if (ncs == kChunkBatch)
           mm_chunks<NT, kChunkBatch, P32>(stage, 0, warp * kRowBlocksPerWarp, lane, acc);
         else
-          mm_chunks<NT, 1, P32>(stage, 0, warp * kRowBlocksPerWarp, lane, acc);
+          for (int u = 0; u < ncs; ++u) mm_chunks<NT, 1, P32>(stage, u, warp * kRowBlocksPerWarp, lane, acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stg]);
       }
