@@ -233,6 +233,21 @@ def run_matmul(args):
     return r
 
 
+def aggregate_replicas(local_ms, local_tokens, world, device):
+    """Whole-job throughput of `world` independent replicas (one sequence per rank, no data
+    exchange): the time is the maximum over ranks of each rank's timed milliseconds, the value
+    every rank's tokens over that time.  Returns (max ms, tokens per second)."""
+    total_ms = float(local_ms)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    return total_ms, local_tokens * world / (total_ms / 1e3)
+
+
 def timed_generate(sess, prompt_dev, max_new, stream, **kw):
     """Prefill (untimed), then one generation timed with CUDA events on the launching stream:
     (tokens/s, tokens, report)."""
@@ -336,14 +351,7 @@ def run_ours(args, rank, world):
             times.append(ms)
             reps.append(rep)
     torch.cuda.synchronize()
-    total_ms = sum(times)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-        torch.distributed.barrier()
-    tokens = MAX_NEW * args.steps * world
-    value = tokens / (total_ms / 1e3)
+    total_ms, value = aggregate_replicas(sum(times), MAX_NEW * args.steps, world, dev)
 
     # end to end through the public call (host prompt -> tokens on the host)
     prompt_list = prompt.tolist()
