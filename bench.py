@@ -52,6 +52,7 @@ WORKLOADS = {
 # the window test: 8B-shaped model, 2048 tokens of 8 motifs of 32 tokens, 30% substitutions
 WINDOW_TEST = ("llama3-8b-shaped", 2048, 8, 32, 0.30, 1005)
 MATMUL_SHAPES = [(896, 4864), (4864, 896), (4096, 14336), (14336, 4096), (4096, 128256)]
+MEM_SUB = 0.30  # replaced fraction of the earlier output held in the window test's session memory
 MATMUL_TOKENS = [1, 2, 4, 8, 16]
 
 
@@ -539,9 +540,34 @@ def run_extras(model8b, torch, stream):
                          "host_syncs": rep.host_syncs, "tau": round(len(toks) / max(1, rep.n_steps), 3),
                          "accepted_drafts_per_step": round(rep.accepted_drafts / max(1, rep.n_steps), 3),
                          "width_steps": {str(w): rep.width_steps[w] for w in WIDTHS}}
-    out["window_test"] = {"model": sh_name, "prompt": "%d tokens, %d motifs x %d, substitution p=%.2f" %
-                          (plen, nmot, mlen, psub), "new_tokens": new, "by_window": runs}
+    # The same test with drafts that can be accepted.  Random-init weights never continue a span
+    # of their context, so the drafts come from the session memory instead: it holds this
+    # request's own greedy output (an earlier answer) with a fraction MEM_SUB of its tokens
+    # replaced by random ones; a draft is accepted up to the next replaced token, so MEM_SUB sets
+    # the acceptance.  The output must still be the greedy one.
+    import numpy as np
+    ref, _ = timed_generate(s, pd, new, stream, window=16, fixed_width=1)[1:]
+    rng = np.random.default_rng(seed + 1)
+    noisy = np.asarray(ref, dtype=np.int64)
+    sub = rng.random(noisy.size) < MEM_SUB
+    noisy[sub] = rng.integers(0, synth.SHAPES[sh_name].vocab, size=int(sub.sum()))
     s.close()
+    sm = W.Session(model8b, plen + new + 64, plen + new + 96, max_window=16, mem_cap=4096)
+    sm.memory_append(noisy.tolist())
+    runs_m = {}
+    for Wn in (1, 4, 16):
+        v, toks, rep = timed_generate(sm, pd, new, stream, window=Wn, widths=WIDTHS, t_us=t_us)
+        runs_m[str(Wn)] = {"tokens_per_s": round(v, 2), "steps": rep.n_steps, "windows": rep.n_windows,
+                           "host_syncs": rep.host_syncs, "tau": round(len(toks) / max(1, rep.n_steps), 3),
+                           "accepted_drafts_per_step": round(rep.accepted_drafts / max(1, rep.n_steps), 3),
+                           "width_steps": {str(w): rep.width_steps[w] for w in WIDTHS},
+                           "equals_greedy": toks == ref}
+    sm.close()
+    out["window_test"] = {"model": sh_name, "prompt": "%d tokens, %d motifs x %d, substitution p=%.2f" %
+                          (plen, nmot, mlen, psub), "new_tokens": new, "by_window": runs,
+                          "with_session_memory": {
+                              "memory": "this request's greedy output with %d%% of its tokens replaced" %
+                                        round(100 * MEM_SUB), "by_window": runs_m}}
     return out
 
 

@@ -73,7 +73,6 @@ struct DecoderBufs {
   float* qkv;             // [kMaxBucket][qkv_rows] (the attention output [kMaxBucket][Hq*D] too)
   float* qrot;            // [kMaxBucket][Hq][D]
   float* gu;              // [kMaxBucket][2F]
-  float* logits;          // [16][V]
   float* o_part;          // attention split partials [chain][split][16][Hq][D] (split < n_chunks, 2 chains)
   float* ml_part;         // [chain][split][16][Hq] (running max, sum)
   uint8_t* act;           // activation records of the next matmul (max K)

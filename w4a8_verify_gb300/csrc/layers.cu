@@ -297,14 +297,15 @@ __global__ void __launch_bounds__(512)
   __shared__ int si[32];
   __shared__ unsigned s_ticket;
   const int t = blockIdx.x, sl = blockIdx.y, ns = gridDim.y;
-  float* lr = logits + (size_t)t * V;
+  float* lr = logits != nullptr ? logits + (size_t)t * V : nullptr;
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   const int k1 = min(V, (sl + 1) * kArgmaxSlice);
-  // the head projection's slices are folded here (V % 4 == 0); the logits are kept for readers
+  // the head projection's slices are folded here (V % 4 == 0); the logits are stored only for
+  // a caller that asked for them
   for (int k = sl * kArgmaxSlice + 4 * threadIdx.x; k < k1; k += 4 * blockDim.x) {
     const float4 v = mm_fold4(lpart, lS, V, t, k, a_s);
-    *reinterpret_cast<float4*>(lr + k) = v;
+    if (lr != nullptr) *reinterpret_cast<float4*>(lr + k) = v;
     if (v.x > bv) { bv = v.x; bi = k; }
     if (v.y > bv) { bv = v.y; bi = k + 1; }
     if (v.z > bv) { bv = v.z; bi = k + 2; }
@@ -460,9 +461,10 @@ cudaError_t launch_swiglu_quant(const DecoderBufs& b, const ModelDims& m, int N,
                     (const float*)b.gu, m.F, 2 * m.F, (const float2*)b.qpart, ns, 0.0f, b.act, N, b.a_s);
 }
 
-cudaError_t launch_argmax(const DecoderBufs& b, const ModelDims& m, int N, int lm_S, cudaStream_t st) {
+cudaError_t launch_argmax(const DecoderBufs& b, const ModelDims& m, int N, int lm_S, float* logits,
+                          cudaStream_t st) {
   return launch_pdl(k_argmax, dim3(N, (m.V + kArgmaxSlice - 1) / kArgmaxSlice), dim3(512), 0, st,
-                    (const SpecCtl*)b.ctl, (const float*)b.mm_part, lm_S, (const float*)b.a_s, b.logits, m.V,
+                    (const SpecCtl*)b.ctl, (const float*)b.mm_part, lm_S, (const float*)b.a_s, logits, m.V,
                     b.argmax_part, b.argmax_tickets, b.pred);
 }
 

@@ -28,8 +28,8 @@ cudaError_t launch_tree_attention(const DecoderBufs& b, const ModelDims& m, int 
 // gate|up from the gu_S EPI_PARTIAL slices in b.mm_part
 cudaError_t launch_swiglu_quant(const DecoderBufs& b, const ModelDims& m, int N, int gu_S, cudaStream_t st);
 // logits from the lm_S EPI_PARTIAL slices of the head projection in b.mm_part (folded here and
-// stored to b.logits)
-cudaError_t launch_argmax(const DecoderBufs& b, const ModelDims& m, int N, int lm_S, cudaStream_t st);
+// stored to `logits` [N][vocab] when it is not null)
+cudaError_t launch_argmax(const DecoderBufs& b, const ModelDims& m, int N, int lm_S, float* logits, cudaStream_t st);
 
 // int8 codes of the current activation records (M tokens, K inputs) -> out [M][K]
 cudaError_t launch_trace_codes(const DecoderBufs& b, int M, int K, int8_t* out, cudaStream_t st);

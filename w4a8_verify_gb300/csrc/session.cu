@@ -197,9 +197,7 @@ cudaError_t forward(w4a8_session* s, int N, bool head, float* logits_out, cudaSt
     TRYC(trace_codes(d.H));
     TRYC(mm_run(m->p_lm, m->lm_w, m->lm_s, b.act, b.a_s, N, nullptr, 0, EPI_PARTIAL, b.mm_part, b.tickets, flags,
                 flags, st));
-    TRYC(launch_argmax(b, d, N, m->p_lm.S, st));
-    if (logits_out)
-      TRYC(cudaMemcpyAsync(logits_out, b.logits, (size_t)N * d.V * sizeof(float), cudaMemcpyDeviceToDevice, st));
+    TRYC(launch_argmax(b, d, N, m->p_lm.S, logits_out, st));
   }
   return cudaSuccess;
 }
@@ -344,7 +342,6 @@ W4A8_API w4a8_status w4a8_session_create(w4a8_model* m, const w4a8_session_desc*
             A.dalloc(&b.pred, kMaxWidth * 4) && A.dalloc(&b.x, (size_t)kMaxBucket * d.H * 4) &&
             A.dalloc(&b.qkv, (size_t)kMaxBucket * std::max(m->qkv_rows, QD) * 4) &&
             A.dalloc(&b.qrot, (size_t)kMaxBucket * QD * 4) && A.dalloc(&b.gu, (size_t)kMaxBucket * 2 * d.F * 4) &&
-            A.dalloc(&b.logits, (size_t)kMaxWidth * d.V * 4) &&
             A.dalloc(&b.o_part, (size_t)kChains * b.n_chunks * kMaxWidth * QD * 4) &&
             A.dalloc(&b.ml_part, (size_t)kChains * b.n_chunks * kMaxWidth * d.Hq * 8) &&
             A.dalloc(&b.act, act_bytes_nt(Kmax, act_tiles(kMaxBucket))) &&
