@@ -206,20 +206,22 @@ def test_verify_n_nodes_bitwise_equals_single_steps(tiny):
             assert torch.equal(lg[node], seq[len(prompt) - 1 + depth]), (leaf, node)
 
 
-def test_trace_does_not_change_the_pass(tiny):
-    """The traced pass computes the same logits, bit for bit, as the plain one."""
+@pytest.mark.parametrize("N", [1, 5, 8, 9])
+def test_trace_does_not_change_the_pass(tiny, N):
+    """The traced pass computes the same logits, bit for bit, as the plain one (one-tile and
+    two-tile widths)."""
     prompt = list(tiny["prompt"])
-    tok, parent = synth.random_tree(np.random.default_rng(3), 9, SHAPE.vocab)
+    tok, parent = synth.random_tree(np.random.default_rng(3 + N), N, SHAPE.vocab)
     out = []
     for traced in (False, True):
         s = _session(tiny)
         s.prefill(_dev(prompt), max_new=8)
         s.set_tree(tok.tolist(), parent.tolist())
         if traced:
-            out.append(P.traced_verify(s, SHAPE, 9)[0])
+            out.append(P.traced_verify(s, SHAPE, N)[0])
         else:
-            lg = torch.empty((9, SHAPE.vocab), dtype=torch.float32, device="cuda")
-            s.tree_verify_step(9, lg)
+            lg = torch.empty((N, SHAPE.vocab), dtype=torch.float32, device="cuda")
+            s.tree_verify_step(N, lg)
             out.append(lg.cpu().numpy())
     assert np.array_equal(out[0], out[1])
 

@@ -5,6 +5,10 @@ Two-layer decoders with the full per-layer dimensions of the benchmarked workloa
   128256 (the headline workload);
 * Qwen2.5-0.5B-shaped: hidden 896, 14 query / 2 KV heads of 64 (7 query heads per KV
   head), FFN 4864, tied vocab 151936.
+A third two-layer model has awkward dimensions for the quantisers and the matmul: hidden
+1120 (the last 64-input chunk of every hidden-wide input is half padding; the O, down and LM
+projections end in a partial row group), FFN 16416 (33 statistics slices per token; a
+half-padded last chunk), 10 query / 2 KV heads of 64 (5 query heads per KV head).
 Weights are seeded int4 codes U{-8..7} with fp16 group scales U(0.001, 0.008) (about the
 spread of N(0, 0.02) weights after quantisation), loaded into the library in the packed
 layout and given to the oracle as the same codes; the cache below the tree is the same
@@ -29,6 +33,7 @@ pytestmark = pytest.mark.gpu
 
 LLAMA_2L = synth.ModelShape("llama3-8b-2layer", 2, 4096, 32, 8, 128, 14336, 14336, 128256, False)
 QWEN_2L = synth.ModelShape("qwen2.5-0.5b-2layer", 2, 896, 14, 2, 64, 4864, 4864, 151936, True)
+EDGE_2L = synth.ModelShape("edge-2layer", 2, 1120, 10, 2, 64, 16416, 16416, 4096, False)
 TALLY = P.Tally()
 CACHE_BYTES = 16 << 30        # the oracle keeps these models' dequantised weights (~8 GB)
 
@@ -75,7 +80,7 @@ def models():
         pytest.skip("no CUDA device")
     W.lib()
     out = {}
-    for shape in (LLAMA_2L, QWEN_2L):
+    for shape in (LLAMA_2L, QWEN_2L, EDGE_2L):
         out[shape.name] = (shape,) + build_pair(shape, 1100 + len(out))
     yield out
     print("\n[benchmarked-shape parity] " + TALLY.summary())
@@ -88,6 +93,17 @@ def test_tree_verify_at_benchmarked_dims(models, name, N, L, seed, monkeypatch):
     monkeypatch.setattr(OM, "DEQ_CACHE_BYTES", CACHE_BYTES)
     rng = np.random.default_rng(seed)
     tok, parent = synth.random_tree(rng, N, shape.vocab, max_depth=8)
+    s = W.Session(m, L + 64, L + 64, 4)
+    s.prefill(torch.as_tensor(synth.motif_prompt(500 + seed, L + 1, 4, 16, 0.1, shape.vocab)).cuda(), max_new=8)
+    P.verify_on_given_cache(s, ow, shape, L, tok, parent, 600 + seed, TALLY)
+    s.close()
+
+
+@pytest.mark.parametrize("N,L,seed", [(1, 130, 10), (5, 300, 11), (8, 257, 12), (16, 300, 13)])
+def test_tree_verify_at_awkward_dims(models, N, L, seed, monkeypatch):
+    shape, m, ow = models[EDGE_2L.name]
+    monkeypatch.setattr(OM, "DEQ_CACHE_BYTES", CACHE_BYTES)
+    tok, parent = synth.random_tree(np.random.default_rng(seed), N, shape.vocab, max_depth=8)
     s = W.Session(m, L + 64, L + 64, 4)
     s.prefill(torch.as_tensor(synth.motif_prompt(500 + seed, L + 1, 4, 16, 0.1, shape.vocab)).cuda(), max_new=8)
     P.verify_on_given_cache(s, ow, shape, L, tok, parent, 600 + seed, TALLY)
