@@ -388,10 +388,11 @@ def run_ours(args, rank, world):
     sess.prefill(prompt_dev, MAX_NEW)
     mm = {}
     for N in (1, 8, 16):
-        if N == 1:
-            torch.cuda.nvtx.range_push("matmul_pass")  # lets a profiler select these launches
+        # NVTX ranges "matmul_pass" (1 token) and "matmul_pass_16" let a profiler select launches
+        if N in (1, 16):
+            torch.cuda.nvtx.range_push("matmul_pass" if N == 1 else "matmul_pass_16")
         us, byts, nl = sess.time_matmuls(N, reps=20)
-        if N == 1:
+        if N in (1, 16):
             torch.cuda.nvtx.range_pop()
         mm[N] = (us, byts, nl)
     us1, bytes1, nl = mm[1]

@@ -516,9 +516,9 @@ def test_cancel_by_terminate_flag(tiny):
 
 # ------------------------------------------------------------------------- edge sizes
 
-@pytest.mark.parametrize("n", [2, 17, 32, 33, 34, 64, 65, 66, 97])
+@pytest.mark.parametrize("n", [2, 17, 33, 64, 65, 66, 97, 129, 130, 145])
 def test_prefill_bucket_edges_equal_sequential_kv(tiny, n):
-    """Prompts whose length puts the prefill on either side of the 32-token bucket edges (and
+    """Prompts whose length puts the prefill on either side of the 64-token bucket edges (and
     the rest on the chain edges) leave the bits of sequential single-token steps."""
     rng = np.random.default_rng(n)
     prompt = rng.integers(0, SHAPE.vocab, size=n).tolist()

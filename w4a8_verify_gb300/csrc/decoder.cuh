@@ -10,7 +10,7 @@
 namespace w4a8 {
 
 constexpr int kMaxWidth = 16;     // tree nodes per step (node 0 = last committed token)
-constexpr int kMaxBucket = 32;    // prompt tokens per prefill bucket (two chains of kMaxWidth for attention)
+constexpr int kMaxBucket = 64;    // prompt tokens per prefill bucket (four chains of kMaxWidth for attention)
 constexpr int kMaxCont = 8;       // drafter continuation length -> at most 9 tokens per step
 constexpr int kAttnChunk = 64;    // logical positions per attention chunk (fixed: part of the order)
 

@@ -45,9 +45,9 @@ __host__ __device__ inline size_t tile_index(int N, int KC, int rb, int c) {
   return (size_t)grp * kGroupBlocks * KC + (size_t)c * nrb + rbl;
 }
 
-// activation records: 8-token tiles for M tokens (1, 2 or 4 tiles: up to 32 tokens), bytes per
-// chunk, buffer bytes for K inputs (act_bytes: up to 16 tokens; act_bytes_nt: NT tiles)
-__host__ __device__ inline int act_tiles(int M) { return M > 16 ? 4 : (M > 8 ? 2 : 1); }
+// activation records: 8-token tiles for M tokens (1, 2, 4 or 8 tiles: up to 64 tokens), bytes
+// per chunk, buffer bytes for K inputs (act_bytes: up to 16 tokens; act_bytes_nt: NT tiles)
+__host__ __device__ inline int act_tiles(int M) { return M > 32 ? 8 : (M > 16 ? 4 : (M > 8 ? 2 : 1)); }
 __host__ __device__ inline int act_rec_bytes(int NT) { return NT * 1152; }
 __host__ __device__ inline size_t act_bytes(int K) { return (size_t)chunks_of(K) * 2 * 1152; }
 __host__ __device__ inline size_t act_bytes_nt(int K, int NT) { return (size_t)chunks_of(K) * NT * 1152; }

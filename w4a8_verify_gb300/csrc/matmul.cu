@@ -124,9 +124,13 @@ template <int NT, int MODE = kModeNormal> constexpr int stage_bytes() {
   return kStageA0 + kChunkBatch * (NT > 2 ? NT : 2) * rec_tile_bytes<MODE>();
 }
 constexpr int kStages = 2;
+// Ring depth per token-tile count.  The 32- and 64-token kernels (134+ registers, 55 / 74 KB
+// stages) fit one CTA per SM: they run a grid of one CTA per SM with a 4- or 3-stage ring (the
+// schedule of units and every accumulation order stay those of the plan).
+template <int NT> constexpr int stages_of() { return NT == 8 ? 3 : (NT == 4 ? 4 : kStages); }
 constexpr int kMmThreads = 32 * (kWarpsPerCta + 1);                  // + one producer warp
 template <int NT, int MODE = kModeNormal> constexpr size_t mm_smem() {
-  return (size_t)kStages * stage_bytes<NT, MODE>();
+  return (size_t)stages_of<NT>() * stage_bytes<NT, MODE>();
 }
 
 // NCH consecutive chunks of one stage for the kRowBlocksPerWarp row blocks from rl0.
@@ -141,17 +145,22 @@ __device__ __forceinline__ void mm_chunks(const uint8_t* stage, int u0, int rl0,
 #pragma unroll
   for (int u = u0; u < u0 + NCH; ++u) {
     const uint8_t* sa = stage + kStageA0 + u * rec;
-    // group gg of the chunk: every row block's accumulators take group 0 before group 1
+    // group gg of the chunk: every row block's accumulators take group 0 before group 1 (the
+    // token tiles in batches of HT; each accumulator sees the same operations in either batch)
+    constexpr int HT = NT > 4 ? 4 : NT;
 #pragma unroll
-    for (int gg = 0; gg < 2; ++gg) {
-      uint4 bf[NT];
-      float4 cq[NT];
-      float2 as2[NT];  // P32: s_a of tokens t0 and t0 + 1 for this group
+    for (int gg = 0; gg < 2; ++gg)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        bf[nt] = reinterpret_cast<const uint4*>(sa + (nt * 2 + gg) * 512)[lane];
-        cq[nt] = reinterpret_cast<const float4*>(sa + NT * 1024 + (gg * NT + nt) * 64)[tig];
-        if (P32) as2[nt] = reinterpret_cast<const float2*>(sa + NT * 1152 + (gg * NT + nt) * 32)[tig];
+    for (int h0 = 0; h0 < NT; h0 += HT) {
+      uint4 bf[HT];
+      float4 cq[HT];
+      float2 as2[HT];  // P32: s_a of tokens t0 and t0 + 1 for this group
+#pragma unroll
+      for (int j = 0; j < HT; ++j) {
+        const int nt = h0 + j;
+        bf[j] = reinterpret_cast<const uint4*>(sa + (nt * 2 + gg) * 512)[lane];
+        cq[j] = reinterpret_cast<const float4*>(sa + NT * 1024 + (gg * NT + nt) * 64)[tig];
+        if (P32) as2[j] = reinterpret_cast<const float2*>(sa + NT * 1152 + (gg * NT + nt) * 32)[tig];
       }
 #pragma unroll
       for (int r = 0; r < kRowBlocksPerWarp; ++r) {
@@ -163,24 +172,25 @@ __device__ __forceinline__ void mm_chunks(const uint8_t* stage, int u0, int rl0,
         uint32_t wa[4], wb[4];
         unpack_codes(wv.x, wa);
         unpack_codes(wv.y, wb);
-        float d[NT][4];
+        float d[HT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_f16(d[nt], wa[0], wb[0], wa[1], wb[1], bf[nt].x, bf[nt].y, cq[nt].x, cq[nt].y, cq[nt].z, cq[nt].w);
+        for (int j = 0; j < HT; ++j)
+          mma_f16(d[j], wa[0], wb[0], wa[1], wb[1], bf[j].x, bf[j].y, cq[j].x, cq[j].y, cq[j].z, cq[j].w);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_f16(d[nt], wa[2], wb[2], wa[3], wb[3], bf[nt].z, bf[nt].w, d[nt][0], d[nt][1], d[nt][2], d[nt][3]);
+        for (int j = 0; j < HT; ++j)
+          mma_f16(d[j], wa[2], wb[2], wa[3], wb[3], bf[j].z, bf[j].w, d[j][0], d[j][1], d[j][2], d[j][3]);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+        for (int j = 0; j < HT; ++j) {
+          const int nt = h0 + j;
           if (P32) {
             float p0, p1, p2, p3;  // s_w * s_a per (row, token), each rounded once
-            mul2(p0, p1, sg.x, as2[nt].x, as2[nt].y);
-            mul2(p2, p3, sg.y, as2[nt].x, as2[nt].y);
-            fma2v(acc[r][nt][0], acc[r][nt][1], p0, p1, d[nt][0], d[nt][1]);
-            fma2v(acc[r][nt][2], acc[r][nt][3], p2, p3, d[nt][2], d[nt][3]);
+            mul2(p0, p1, sg.x, as2[j].x, as2[j].y);
+            mul2(p2, p3, sg.y, as2[j].x, as2[j].y);
+            fma2v(acc[r][nt][0], acc[r][nt][1], p0, p1, d[j][0], d[j][1]);
+            fma2v(acc[r][nt][2], acc[r][nt][3], p2, p3, d[j][2], d[j][3]);
           } else {
-            fma2(acc[r][nt][0], acc[r][nt][1], sg.x, d[nt][0], d[nt][1]);
-            fma2(acc[r][nt][2], acc[r][nt][3], sg.y, d[nt][2], d[nt][3]);
+            fma2(acc[r][nt][0], acc[r][nt][1], sg.x, d[j][0], d[j][1]);
+            fma2(acc[r][nt][2], acc[r][nt][3], sg.y, d[j][2], d[j][3]);
           }
         }
       }
@@ -191,7 +201,7 @@ __device__ __forceinline__ void mm_chunks(const uint8_t* stage, int u0, int rl0,
 // Persistent CTAs: kWarpsPerCta consumer warps (kRowBlocksPerWarp 16-row blocks each) and one
 // producer warp.  Work units (row group g, K slice s), unit w = g*S + s, are dealt round-robin to
 // the CTAs.  The producer streams, per stage of kChunkBatch 64-input chunks, the row group's
-// weights and scales and the activation records into a kStages-deep shared-memory ring with
+// weights and scales and the activation records into a stages_of<NT>()-deep shared-memory ring with
 // cp.async.bulk, continuing across units; weight copies of the first stages are issued before
 // griddepcontrol.wait (weights are constant), activations only after it.  A unit's result is
 // folded with the other slices of its row group by the last unit to finish (ticket), in
@@ -212,7 +222,8 @@ __global__ void __launch_bounds__(kMmThreads)
   constexpr bool FAULT = MODE == kModeFault;
   constexpr bool P32 = MODE == kModePer32;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint64_t full[kStages], empty[kStages];
+  constexpr int ST = stages_of<NT>();
+  __shared__ uint64_t full[ST], empty[ST];
   __shared__ unsigned s_ticket;
   constexpr int rec = NT * rec_tile_bytes<MODE>();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -223,7 +234,7 @@ __global__ void __launch_bounds__(kMmThreads)
   // grid to complete
   griddep_launch();
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < ST; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kWarpsPerCta);
     }
@@ -257,7 +268,7 @@ __global__ void __launch_bounds__(kMmThreads)
       auto issue_weights = [&](Pos ps, int it) {
         int g, cb, nc, nrb;
         batch_info(ps, g, cb, nc, nrb);
-        const int stg = it % kStages;
+        const int stg = it % ST;
         mbar_expect_tx(&full[stg], (unsigned)(nc * nrb * 576 + nc * rec));
         uint8_t* s0 = smem + (size_t)stg * stage_bytes<NT, MODE>();
         const size_t t0 = tile_index(N, KC, g * kGroupBlocks, cb);
@@ -275,15 +286,15 @@ __global__ void __launch_bounds__(kMmThreads)
       auto issue_acts = [&](Pos ps, int it) {
         int g, cb, nc, nrb;
         batch_info(ps, g, cb, nc, nrb);
-        const int stg = it % kStages;
+        const int stg = it % ST;
         bulk_g2s(smem + (size_t)stg * stage_bytes<NT, MODE>() + kStageA0, act + (size_t)cb * rec, (unsigned)(nc * rec),
                  &full[stg]);
       };
-      Pos pro[kStages];
+      Pos pro[ST];
       int npro = 0;
       Pos ps{(int)blockIdx.x, 0};
       if (FAULT) ps.w = units;  // nothing is issued
-      while (npro < kStages && ps.w < units) {
+      while (npro < ST && ps.w < units) {
         issue_weights(ps, npro);
         pro[npro++] = ps;
         ps = next(ps);
@@ -293,8 +304,8 @@ __global__ void __launch_bounds__(kMmThreads)
       for (int i = 0; i < npro; ++i) issue_acts(pro[i], i);  // complete the in-flight stages
       if (stop == nullptr || !(__ldcg(stop) & FLAG_STOP_MASK)) {
         for (int it = npro; ps.w < units && ok; ++it) {
-          const int stg = it % kStages;
-          ok = mbar_wait(&empty[stg], ((it / kStages) - 1) & 1);
+          const int stg = it % ST;
+          ok = mbar_wait(&empty[stg], ((it / ST) - 1) & 1);
           if (!ok) {
             atomicOr(err, FLAG_ERR_TIMEOUT);
             break;
@@ -306,8 +317,8 @@ __global__ void __launch_bounds__(kMmThreads)
         }
       }
       // drain: every issued stage must land before the CTA may exit
-      for (int it = max(0, issued - kStages); it < issued; ++it) {
-        if (!mbar_wait(&full[it % kStages], (it / kStages) & 1)) {
+      for (int it = max(0, issued - ST); it < issued; ++it) {
+        if (!mbar_wait(&full[it % ST], (it / ST) & 1)) {
           atomicOr(err, FLAG_ERR_TIMEOUT);
           break;
         }
@@ -334,8 +345,8 @@ __global__ void __launch_bounds__(kMmThreads)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[r][nt][e] = 0.0f;
       for (int b = 0; b < nb; ++b, ++it) {
-        const int stg = it % kStages;
-        if (ok && !mbar_wait(&full[stg], (it / kStages) & 1, FAULT ? kFaultWaitNs : kWaitLimitNs)) {
+        const int stg = it % ST;
+        if (ok && !mbar_wait(&full[stg], (it / ST) & 1, FAULT ? kFaultWaitNs : kWaitLimitNs)) {
           if (lane == 0) atomicOr(err, FLAG_ERR_TIMEOUT);
           ok = false;
         }
@@ -484,6 +495,8 @@ cudaError_t mm_configure() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_mm<4, kModeNormal>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mm_smem<4, kModeNormal>());
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_mm<8, kModeNormal>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mm_smem<8, kModeNormal>());
+  if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_mm<1, kModeFault>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mm_smem<1, kModeNormal>());
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_mm<2, kModeFault>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mm_smem<2, kModeNormal>());
@@ -509,9 +522,13 @@ cudaError_t mm_run(const MatmulPlan& p, const uint32_t* wt, const uint16_t* st, 
   if (act_tiles(M) == 2)
     return launch_pdl(k_mm<2, kModeNormal>, grid, block, mm_smem<2, kModeNormal>(), stream, w8, s8, act, a_s, M, p.N, ldy, p.KC, p.cps,
                       p.S, y, epi, part, tickets, err, stop);
-  // 17..32 tokens (prefill buckets): split-K partials only (the in-kernel fold of the ticket path
+  // 17..64 tokens (prefill buckets): split-K partials only (the in-kernel fold of the ticket path
   // holds 16 token rows)
   if (epi != EPI_PARTIAL) return cudaErrorInvalidValue;
+  grid.x = (unsigned)(units < kPersistentCtas / 2 ? units : kPersistentCtas / 2);  // one CTA per SM
+  if (act_tiles(M) == 8)
+    return launch_pdl(k_mm<8, kModeNormal>, grid, block, mm_smem<8, kModeNormal>(), stream, w8, s8, act, a_s, M, p.N,
+                      ldy, p.KC, p.cps, p.S, y, epi, part, tickets, err, stop);
   return launch_pdl(k_mm<4, kModeNormal>, grid, block, mm_smem<4, kModeNormal>(), stream, w8, s8, act, a_s, M, p.N, ldy, p.KC, p.cps,
                     p.S, y, epi, part, tickets, err, stop);
 }

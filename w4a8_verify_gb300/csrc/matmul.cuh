@@ -23,8 +23,8 @@ constexpr int kRowsPerCta = 16 * kWarpsPerCta * kRowBlocksPerWarp;  // 256
 MatmulPlan mm_plan(int K, int N);
 
 // Token rows of the EPI_PARTIAL layout (the widest token count a decoder pass uses: a prefill
-// bucket of 32 prompt tokens).
-constexpr int kPartTokens = 32;
+// bucket of 64 prompt tokens).
+constexpr int kPartTokens = 64;
 // floats of the EPI_PARTIAL output of a plan: [S][kPartTokens][N]
 inline size_t mm_partial_floats(const MatmulPlan& p) { return (size_t)p.S * kPartTokens * p.N; }
 

@@ -417,10 +417,10 @@ W4A8_API w4a8_status w4a8_prefill(w4a8_session* s, const int32_t* prompt, int n,
   cudaStream_t st = as_stream(stream);
   W4A8_CUDA_TRY(cudaMemcpyAsync(b.ctx, prompt, (size_t)n * 4, cudaMemcpyDeviceToDevice, st));
   W4A8_CUDA_TRY(launch_pdl(k_init_ctl, dim3(1), dim3(32), 0, st, b.ctl, b.rec, (const int32_t*)b.ctx, n, max_new));
-  // Integer prefill in wide buckets [P1 Small-Batch Verification Kernels: bucket of 32 tokens;
-  // Experiments: request latency]: full buckets of kMaxBucket prompt tokens replay one captured
-  // graph (the kernels read their position from the control word): the matmuls and the row-wise
-  // kernels take the whole bucket, the attention its two chains of kMaxWidth.  The rest runs as
+  // Integer prefill in wide buckets [P1 Small-Batch Verification Kernels (token buckets);
+  // Experiments: request latency]: full buckets of kMaxBucket (64) prompt tokens replay one
+  // captured graph (the kernels read their position from the control word): the matmuls and the
+  // row-wise kernels take the whole bucket, the attention its four chains of kMaxWidth.  The rest runs as
   // chains of up to kMaxWidth nodes through the verification kernels.  Every step of a token's
   // forward is row-local with the same order, so the cache holds the bits of sequential steps.
   // (models whose query heads do not share KV heads keep chains of kMaxWidth: their attention
