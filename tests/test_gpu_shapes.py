@@ -110,6 +110,35 @@ def test_tree_verify_at_awkward_dims(models, N, L, seed, monkeypatch):
     s.close()
 
 
+@pytest.mark.parametrize("name", [LLAMA_2L.name, QWEN_2L.name, EDGE_2L.name])
+def test_prefill_buckets_equal_sequential_kv_at_benchmarked_dims(models, name):
+    """145 prompt tokens prefill as two 64-token buckets (the attention as four 16-node chains,
+    with 4, 7 and 5 query heads per KV head) and chains of 16 and 1; the cache must hold the
+    bits that 145 single-token steps write."""
+    shape, m, _ = models[name]
+    n = 146
+    prompt = synth.motif_prompt(77, n, 4, 16, 0.1, shape.vocab)
+    s = W.Session(m, n + 64, n + 64, 4)
+    s.prefill(torch.as_tensor(prompt).cuda(), max_new=8)
+    q = W.Session(m, n + 64, n + 64, 4)
+    q.prefill(torch.as_tensor(prompt[:1]).cuda(), max_new=n + 4)
+    for tok in prompt[:n - 1]:               # teacher-forced single-token steps
+        q.set_tree([int(tok)], [-1])
+        q.tree_verify_step(1)
+        q.accept_greedy(1)
+    L = n - 1
+    for layer in range(shape.n_layers):
+        k1, v1, k2, v2 = (torch.empty((shape.n_kv_heads, L, shape.head_dim), dtype=torch.float32, device="cuda")
+                          for _ in range(4))
+        s.copy_kv(layer, 0, L, k1, v1)
+        q.copy_kv(layer, 0, L, k2, v2)
+        torch.cuda.synchronize()
+        assert torch.equal(k1, k2) and torch.equal(v1, v2), (name, layer)
+    assert s.ctl().committed_len == L and q.ctl().committed_len == L
+    s.close()
+    q.close()
+
+
 def test_tree_verify_at_full_context_8b(models, monkeypatch):
     """One node after a 4095-slot cache at the 8B dimensions (the headline context)."""
     shape, m, ow = models[LLAMA_2L.name]
