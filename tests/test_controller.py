@@ -59,6 +59,30 @@ def test_probe_spacing_follows_costs():
     assert spacing(1.2) < spacing(4.0)
 
 
+def test_failed_probes_back_off_and_an_accepting_probe_resets():
+    c = W.Controller([1, 4], [100.0, 110.0])             # base spacing ceil(4 * 1.1) = 5
+    for _ in range(20):
+        c.observe(4, [st(0, 0, 1)] * 4)                  # wide windows accept nothing: plain is best
+    gaps, last = [], 0
+    for k in range(1, 400):
+        w = c.choose()
+        if w == 4:
+            gaps.append(k - last)
+            last = k
+            c.observe(4, [st(0, 0, 1)])                  # the probe accepts no draft
+        else:
+            c.observe(1, [st(0, 0, 1)])
+    assert gaps[:5] == [5, 10, 20, 40, 64] and all(g == 64 for g in gaps[5:])
+    # a probe that accepts a draft returns the spacing to the cost-based one
+    while c.choose() != 4:
+        c.observe(1, [st(0, 0, 1)])
+    c.observe(4, [st(1, 1, 2)])
+    n = 1
+    while c.choose() != 4:
+        n += 1
+    assert n == 5
+
+
 def test_cost_moving_average():
     c = W.Controller([1, 4], [100.0, 200.0])
     c.observe(4, [st(1, 1)] * 4, interval_us=4 * 120.0)

@@ -12,8 +12,9 @@
 //
 // Readings (the page gives no constants): history of the last 32 steps; prior of 2
 // pseudo-steps at 1 + 0.5 * min(N - 1, match length) tokens; a match length of 2 assumed
-// before any step; probe spacing ceil(4 * T(N_2) / T(N_1)) windows clamped to [2, 64];
-// moving-average weight 0.25.
+// before any step; probe spacing ceil(4 * T(N_2) / T(N_1)) windows clamped to [2, 64], doubled
+// (up to 64) after each probe that accepts no draft and reset by one that accepts any, as a
+// congestion controller backs off; moving-average weight 0.25.
 #include <algorithm>
 #include <cmath>
 #include <deque>
@@ -38,7 +39,9 @@ struct w4a8_controller {
   std::vector<double> sum_tok, cnt;  // [width index][match length 0..8]
   std::deque<int> recent;
   int low_streak = 0;
-  int probe_every = 4;
+  int base_every = 4;      // probe spacing from the measured costs
+  int probe_every = 4;     // current spacing (backs off after failed probes)
+  int pending_probes = 0;  // probes chosen whose windows have not been observed
   bool probing = false;
 
   double prior(int w, int ell) const { return 1.0 + kPriorPerMatch * std::min(w - 1, ell); }
@@ -86,7 +89,8 @@ W4A8_API w4a8_status w4a8_controller_create(const int* widths, const float* t_us
   c->cnt.assign((size_t)n * (kMaxLen + 1), 0.0);
   if (n > 1) {
     const double ratio = c->cost[1] / c->cost[0];
-    c->probe_every = std::min(64, std::max(2, (int)std::ceil(4.0 * ratio)));
+    c->base_every = std::min(64, std::max(2, (int)std::ceil(4.0 * ratio)));
+    c->probe_every = c->base_every;
   }
   *out = c;
   return W4A8_OK;
@@ -102,6 +106,7 @@ W4A8_API int w4a8_controller_choose(w4a8_controller* c) {
     if (++c->low_streak >= c->probe_every) {
       c->low_streak = 0;
       c->probing = true;
+      ++c->pending_probes;
       b = 1;  // probe the next wider tree once
     }
   } else {
@@ -114,6 +119,14 @@ W4A8_API w4a8_status w4a8_controller_observe(w4a8_controller* c, int width, cons
                                              double interval_us) {
   if (!c || (n > 0 && !stats) || n < 0) return W4A8_ERR_ARG;
   const int i = c->index_of(width);
+  if (i == 1 && n > 0 && c->pending_probes > 0) {
+    // the window of a probe (windows complete in the order they were chosen): back off while
+    // probes find nothing to accept, return to the cost-based spacing when one does
+    --c->pending_probes;
+    int accepted = 0;
+    for (int k = 0; k < n; ++k) accepted += std::max(0, (int)stats[k].n_emitted - 1);
+    c->probe_every = accepted > 0 ? c->base_every : std::min(64, 2 * c->probe_every);
+  }
   for (int k = 0; k < n; ++k) {
     const int ell = std::min<int>(kMaxLen, stats[k].best_match_len);
     if (i >= 0 && stats[k].n_emitted > 0) {
