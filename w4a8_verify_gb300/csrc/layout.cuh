@@ -15,7 +15,7 @@
 // 16n * 2^-24.  Pairs p = 1, 3 carry the extra factor 16, which the activation side
 // cancels by holding a/16 for those inputs.
 //
-// Activation records.  For NT 8-token tiles (NT = 1 for up to 8 tokens, 2 up to 16, 4 up to 32) the
+// Activation records.  For NT 8-token tiles (NT = 1 for up to 8 tokens, 2 up to 16, 4 up to 32, 8 up to 64) the
 // record of chunk c is NT * 1152 bytes at offset c * NT * 1152:
 //   [nt][group 0..1][lane] uint4 {h2(a_k, a_k+1), h2(a_k+8, a_k+9)/16,
 //                                h2(a_k+16, a_k+17), h2(a_k+24, a_k+25)/16},

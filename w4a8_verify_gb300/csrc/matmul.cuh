@@ -110,7 +110,7 @@ cudaError_t act_prep_run(const int8_t* a_q, int M, int K, int lda, uint8_t* act,
 
 // Device helpers for fused producers of the activation records (layout.cuh), for M tokens
 // (NT = act_tiles(M) tiles).
-// act_store_quad: token t (< 16), inputs k0..k0+3 (k0 % 4 == 0), int8 codes in `codes`
+// act_store_quad: token t (< 8 * NT), inputs k0..k0+3 (k0 % 4 == 0), int8 codes in `codes`
 // (byte b = input k0+b): writes the two f16x2 words that hold them.
 __device__ __forceinline__ void act_store_quad(uint8_t* act, int NT, int t, int k0, uint32_t codes) {
   const int g = k0 >> 5, kin = k0 & 31;
