@@ -271,8 +271,9 @@ void w4a8_session_destroy(w4a8_session* s);
 
 /* Device.  Starts a generation: context = prompt[0..n) (device int32), KV of
  * prompt[0..n-1) computed through the verification kernels in buckets of 64 tokens (the
- * matmuls and row-wise kernels take a whole bucket, the attention four chains of 16) and
- * the rest in chains of up to 16 tokens ("GPU-Resident Speculative Decoding ...", Design >
+ * matmuls and row-wise kernels take a whole bucket, the attention four chains of 16), the
+ * rest as one pass over its whole chains of 16 and one shorter chain
+ * ("GPU-Resident Speculative Decoding ...", Design >
  * Small-Batch Verification Kernels: token buckets), root = prompt[n-1], n_generated = 0,
  * then the first draft tree.  The cache holds the bits of sequential single-token steps. */
 w4a8_status w4a8_prefill(w4a8_session* s, const int32_t* prompt, int n, int max_new, void* stream);

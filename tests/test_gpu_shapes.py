@@ -111,12 +111,13 @@ def test_tree_verify_at_awkward_dims(models, N, L, seed, monkeypatch):
 
 
 @pytest.mark.parametrize("name", [LLAMA_2L.name, QWEN_2L.name, EDGE_2L.name])
-def test_prefill_buckets_equal_sequential_kv_at_benchmarked_dims(models, name):
-    """145 prompt tokens prefill as two 64-token buckets (the attention as four 16-node chains,
-    with 4, 7 and 5 query heads per KV head) and chains of 16 and 1; the cache must hold the
-    bits that 145 single-token steps write."""
+@pytest.mark.parametrize("n", [146, 176])
+def test_prefill_buckets_equal_sequential_kv_at_benchmarked_dims(models, name, n):
+    """n - 1 prompt tokens prefill as two 64-token buckets (the attention as four 16-node chains,
+    with 4, 7 and 5 query heads per KV head), then 145: chains of 16 and 1; 175: one pass over
+    two chains (32 tokens) and a chain of 15.  The cache must hold the bits that n - 1
+    single-token steps write."""
     shape, m, _ = models[name]
-    n = 146
     prompt = synth.motif_prompt(77, n, 4, 16, 0.1, shape.vocab)
     s = W.Session(m, n + 64, n + 64, 4)
     s.prefill(torch.as_tensor(prompt).cuda(), max_new=8)

@@ -150,8 +150,8 @@ size_t trace_bytes(const ModelDims& d, int N) {
 
 // trace: optional device buffer of trace_bytes(d, N) bytes receiving the int8 codes of every
 // quantisation point (tests and tools; not used by the decoding loop).
-// chain: a prefill bucket of N = kMaxBucket context tokens from committed_len (the current tree
-// must be the chain of kMaxWidth nodes, which the attention takes for each half of the bucket);
+// chain: N (a multiple of kMaxWidth, at most kMaxBucket) context tokens from committed_len (the
+// current tree must be the chain of kMaxWidth nodes, which the attention takes for each chain);
 // otherwise the current tree's first N nodes.
 cudaError_t forward(w4a8_session* s, int N, bool head, float* logits_out, cudaStream_t st, int8_t* trace = nullptr,
                     bool chain = false) {
@@ -420,9 +420,10 @@ W4A8_API w4a8_status w4a8_prefill(w4a8_session* s, const int32_t* prompt, int n,
   // Integer prefill in wide buckets [P1 Small-Batch Verification Kernels (token buckets);
   // Experiments: request latency]: full buckets of kMaxBucket (64) prompt tokens replay one
   // captured graph (the kernels read their position from the control word): the matmuls and the
-  // row-wise kernels take the whole bucket, the attention its four chains of kMaxWidth.  The rest runs as
-  // chains of up to kMaxWidth nodes through the verification kernels.  Every step of a token's
-  // forward is row-local with the same order, so the cache holds the bits of sequential steps.
+  // row-wise kernels take the whole bucket, the attention its four chains of kMaxWidth.  Two or
+  // three whole chains left over run as one such pass, the rest as one chain of fewer nodes.
+  // Every step of a token's forward is row-local with the same order, so the cache holds the
+  // bits of sequential steps.
   // (models whose query heads do not share KV heads keep chains of kMaxWidth: their attention
   // merges inside the chunk kernel, which takes one chain per launch)
   const int buckets = d_ok_for_buckets(s->m->d) ? (n - 1) / kMaxBucket : 0;
@@ -444,6 +445,14 @@ W4A8_API w4a8_status w4a8_prefill(w4a8_session* s, const int32_t* prompt, int n,
   }
   for (int c = 0; c < buckets; ++c) W4A8_CUDA_TRY(cudaGraphLaunch(s->bucket_graph, st));
   int done = buckets * kMaxBucket;
+  // two or three whole chains left: one pass over them, as in a bucket (not captured)
+  const int whole = d_ok_for_buckets(s->m->d) ? ((n - 1 - done) / kMaxWidth) * kMaxWidth : 0;
+  if (whole >= 2 * kMaxWidth) {
+    W4A8_CUDA_TRY(launch_chain_tree(b, 0, kMaxWidth, st));
+    W4A8_CUDA_TRY(forward(s, whole, false, nullptr, st, nullptr, true));
+    W4A8_CUDA_TRY(launch_commit_chain(b, whole, st));
+    done += whole;
+  }
   while (done < n - 1) {
     const int len = std::min(kMaxWidth, n - 1 - done);
     W4A8_CUDA_TRY(launch_chain_tree(b, done, len, st));
