@@ -191,7 +191,9 @@ int w4a8_matmul_slices(int K, int N);
 /* Shape of a Llama/Qwen-style decoder without biases, RMSNorm gain 1, rotate-half RoPE
  * [P1 Experiments (models); Implementation].  hidden % 32 == 0, ffn % 32 == 0,
  * (n_heads + 2 n_kv_heads) * head_dim % 16 == 0, head_dim in {64, 128},
- * n_heads % n_kv_heads == 0, n_heads / n_kv_heads <= 8, vocab % 16 == 0. */
+ * n_heads % n_kv_heads == 0, n_heads / n_kv_heads <= 8 (<= 4 at head_dim 128: the tree
+ * attention of 16 nodes holds all query heads of a KV head in one CTA's shared memory),
+ * vocab % 16 == 0; else W4A8_ERR_SHAPE. */
 typedef struct {
   int n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
   int tied;         /* 1: the LM head is the embedding table */

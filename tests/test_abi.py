@@ -66,3 +66,21 @@ def test_matmul_schedule_depends_on_shape_only(lib):
     for K, N in [(896, 4864), (4864, 896), (4096, 14336), (14336, 4096), (4096, 128256), (256, 512), (704, 256)]:
         S = W.w4a8_matmul_slices(K, N)
         assert 1 <= S <= max(1, (K + 63) // 64 // 2)
+
+
+def test_model_shapes_the_tree_attention_cannot_hold_are_rejected(lib):
+    """Head size 128 with more than 4 query heads per KV head needs more than a block's shared
+    memory in the 16-node tree attention: model creation says so (W4A8_ERR_SHAPE) before any
+    device allocation; the benchmarked grouping (4 per KV head at 128, 7 at 64) stays valid."""
+    def create(n_heads, n_kv_heads, head_dim):
+        d = W.ModelDesc(1, 512, n_heads, n_kv_heads, head_dim, 1024, 4096, 0, 1e-6, 10000.0)
+        h = ctypes.c_void_p()
+        st = lib.w4a8_model_create(ctypes.byref(d), ctypes.byref(h))
+        if st == 0:
+            lib.w4a8_model_destroy(h)
+        return st
+    assert create(40, 8, 128) == 2         # 5 per KV head at 128
+    assert create(28, 4, 128) == 2         # 7 per KV head at 128
+    assert create(64, 8, 128) == 2         # 8 per KV head at 128
+    assert create(8, 1, 64) != 2           # 8 per KV head at 64 fits
+    assert create(32, 8, 128) != 2         # 4 per KV head at 128 fits

@@ -226,6 +226,11 @@ W4A8_API w4a8_status w4a8_model_create(const w4a8_model_desc* desc, w4a8_model**
   if (d.hidden % 32 || d.ffn % 32 || d.vocab % 16 || d.n_heads % d.n_kv_heads) return W4A8_ERR_SHAPE;
   if (d.head_dim != 64 && d.head_dim != 128) return W4A8_ERR_SHAPE;
   if (d.n_heads / d.n_kv_heads > 8) return W4A8_ERR_SHAPE;
+  // the attention's dynamic shared memory for 16 nodes x all query heads of a KV head, plus
+  // room for its static arrays, within one block's opt-in limit (227 KB)
+  constexpr size_t kMaxSmemPerBlock = 232448, kAttnStaticRoom = 4096;
+  if (attn_smem_bytes(d.head_dim, kMaxWidth * (d.n_heads / d.n_kv_heads)) + kAttnStaticRoom > kMaxSmemPerBlock)
+    return W4A8_ERR_SHAPE;
   if (((d.n_heads + 2 * d.n_kv_heads) * d.head_dim) % 16) return W4A8_ERR_SHAPE;
   if (!(d.rms_eps >= 0.0f) || !(d.rope_base > 0.0f)) return W4A8_ERR_ARG;
   w4a8_model* m = new (std::nothrow) w4a8_model();
