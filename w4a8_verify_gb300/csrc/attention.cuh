@@ -765,15 +765,9 @@ __global__ void __maxnreg__(168)
     const int smax = ((L + s_dep[i]) / CH) / R;  // splits that saw this node
     const size_t hb = (size_t)i * Hq + kh * G + g;
     const size_t sstride = (size_t)kMaxWidth * Hq;
-    float M = -INFINITY;
-    for (int s2 = lane; s2 <= smax; s2 += 32) M = fmaxf(M, __ldcg(&ml_part[s2 * sstride + hb].x));
-    M = warp_max(M);
-    float Ls = 0.0f, O[DL];
-#pragma unroll
-    for (int d = 0; d < DL; ++d) O[d] = 0.0f;
-    for (int sb = 0; sb <= smax; sb += 8) {
-      float2 ml[8];
-      float ov[8][DL];
+    float2 ml[8];
+    float ov[8][DL];
+    auto load_batch = [&](int sb) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         if (sb + k > smax) break;
@@ -782,6 +776,16 @@ __global__ void __maxnreg__(168)
 #pragma unroll
         for (int d = 0; d < DL; ++d) ov[k][d] = __ldcg(src + d);
       }
+    };
+    load_batch(0);  // in flight together with the loads of the maximum
+    float M = -INFINITY;
+    for (int s2 = lane; s2 <= smax; s2 += 32) M = fmaxf(M, __ldcg(&ml_part[s2 * sstride + hb].x));
+    M = warp_max(M);
+    float Ls = 0.0f, O[DL];
+#pragma unroll
+    for (int d = 0; d < DL; ++d) O[d] = 0.0f;
+    for (int sb = 0; sb <= smax; sb += 8) {
+      if (sb > 0) load_batch(sb);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         if (sb + k > smax) break;

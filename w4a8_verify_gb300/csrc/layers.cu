@@ -94,11 +94,28 @@ __global__ void __launch_bounds__(kQuantSlice / 4)
                                                    fmaxf(fmaxf(s_mx[0], s_mx[1]), fmaxf(s_mx[2], s_mx[3])));
 }
 
-// Quantiser scale of token t from slice maxima (the exact maximum of the partial maxima).
-__device__ __forceinline__ float quant_scale_max(const float2* part, int t, int nparts) {
-  float mx = 0.0f;
-  for (int p = 0; p < nparts; ++p) mx = fmaxf(mx, __ldcg(part + (size_t)t * nparts + p).y);
-  return __fdiv_rn(mx, 127.0f);
+// (sum of .x in ascending p, maximum of .y) over the nparts slice partials of token t.  Lane j
+// of the (whole) warp loads partials j and j + 32, so up to 64 partials cost one round trip;
+// the warp folds the shuffled values in ascending order (later partials are loaded in turn).
+__device__ __forceinline__ float2 fold_partials(const float2* __restrict__ part, int t, int nparts) {
+  const int lane = threadIdx.x & 31;
+  const float2* pr = part + (size_t)t * nparts;
+  const float2 z = make_float2(0.0f, 0.0f);
+  const float2 p0 = lane < nparts ? __ldcg(pr + lane) : z;
+  const float2 p1 = lane + 32 < nparts ? __ldcg(pr + lane + 32) : z;
+  float ss = 0.0f, mx = 0.0f;
+  const int n0 = min(nparts, 64);
+  for (int p = 0; p < n0; ++p) {
+    const float2 v = p < 32 ? p0 : p1;
+    ss = ss + __shfl_sync(0xffffffffu, v.x, p & 31);
+    mx = fmaxf(mx, __shfl_sync(0xffffffffu, v.y, p & 31));
+  }
+  for (int p = 64; p < nparts; ++p) {
+    const float2 v = __ldcg(pr + p);
+    ss = ss + v.x;
+    mx = fmaxf(mx, v.y);
+  }
+  return make_float2(ss, mx);
 }
 
 // int8 codes of the quad (inputs k..k+3 of token t) into the activation records.  Called by a
@@ -136,17 +153,12 @@ __global__ void k_quant_slices(const SpecCtl* ctl, const float* __restrict__ x, 
   if (stopped(ctl)) return;
   const int t = blockIdx.x, sl = blockIdx.y;
   float s, r = 1.0f;
+  const float2 f = fold_partials(part, t, nparts);  // whole warps (128 threads)
   if (MODE == 1) {
-    float mx = 0.0f, ss = 0.0f;
-    for (int p = 0; p < nparts; ++p) {
-      const float2 v = part[(size_t)t * nparts + p];
-      ss = ss + v.x;
-      mx = fmaxf(mx, v.y);
-    }
-    r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
-    s = __fdiv_rn(mx * r, 127.0f);
+    r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(f.x, (float)K), eps)));
+    s = __fdiv_rn(f.y * r, 127.0f);
   } else {
-    s = quant_scale_max(part, t, nparts);
+    s = __fdiv_rn(f.y, 127.0f);  // the exact maximum of the partial maxima
   }
   const int k = sl * kQuantSlice + 4 * threadIdx.x;
   const bool active = k < K;  // K % 32 == 0: groups of 8 lanes are all active or all idle
@@ -216,20 +228,30 @@ __global__ void k_attn_merge(const SpecCtl* ctl, const TreeState* __restrict__ t
   const size_t hb = (size_t)i * Hq + h;
   const size_t ho = (size_t)it * Hq + h;
   const size_t sstride = (size_t)kMaxWidth * Hq;
-  float M = -INFINITY;
-  for (int s2 = 0; s2 <= smax; ++s2) M = fmaxf(M, ml_part[s2 * sstride + hb].x);
-  float Ls = 0.0f, O = 0.0f;
-  for (int sb = 0; sb <= smax; sb += 8) {
-    float2 ml[8];
-    float ov[8];
+  // the partials of splits sb .. sb + MB - 1; the maximum is taken over the first batch as it
+  // arrives and over the later splits' own loads, so up to MB splits cost one round trip
+  constexpr int MB = 16;
+  float2 ml[MB];
+  float ov[MB];
+  auto load_batch = [&](int sb) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < MB; ++k) {
       if (sb + k > smax) break;
       ml[k] = ml_part[(sb + k) * sstride + hb];
       ov[k] = o_part[((sb + k) * sstride + hb) * D + dd];
     }
+  };
+  load_batch(0);
+  float M = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < MB; ++k)
+    if (k <= smax) M = fmaxf(M, ml[k].x);
+  for (int s2 = MB; s2 <= smax; ++s2) M = fmaxf(M, ml_part[s2 * sstride + hb].x);
+  float Ls = 0.0f, O = 0.0f;
+  for (int sb = 0; sb <= smax; sb += MB) {
+    if (sb > 0) load_batch(sb);
+#pragma unroll
+    for (int k = 0; k < MB; ++k) {
       if (sb + k > smax) break;
       const float w = expf(ml[k].x - M);
       Ls = fmaf(w, ml[k].y, Ls);
