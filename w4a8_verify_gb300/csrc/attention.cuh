@@ -420,7 +420,7 @@ __global__ void __maxnreg__(168)
             krow[i] = j < jc ? Ks + (size_t)j * KSTR
                              : (P0 + j - L <= maxd ? Kt + (size_t)s_row[P0 + j - L] * D : nullptr);
           }
-#pragma unroll
+#pragma unroll 1
           for (int st = 0; st < KS; ++st) {
             const uint4* af = reinterpret_cast<const uint4*>(Qf + ((size_t)(mw * KS + st) * 32 + lane) * 32);
             const uint4 ah = af[0], al = af[1];
@@ -496,7 +496,7 @@ __global__ void __maxnreg__(168)
             for (int mi = 0; mi < MSPAN; ++mi)
 #pragma unroll
               for (int e = 0; e < 4; ++e) acc[k][mi][e] = 0.0f;
-#pragma unroll
+#pragma unroll 1
           for (int st = 0; st < KS; ++st) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
