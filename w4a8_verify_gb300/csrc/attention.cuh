@@ -691,7 +691,7 @@ __global__ void __maxnreg__(168)
               if (m < glo || m > ghi) continue;
               const uint4* af = reinterpret_cast<const uint4*>(EF + ((size_t)(m * VS + st) * 32 + lane) * 8);
               const uint4 ah = af[0], al = af[1];
-#pragma unroll
+#pragma unroll 1
               for (int k = 0; k < 4; ++k) {
                 const int node = nb + k;
                 if (node > nlast || m < (node * G) / 16 || m > (node * G + G - 1) / 16) continue;
