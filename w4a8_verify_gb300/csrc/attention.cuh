@@ -449,7 +449,7 @@ __global__ void __maxnreg__(168)
         for (int m = 0; m < MT; ++m)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[m][e] = 0.0f;
-#pragma unroll
+#pragma unroll 1
         for (int st = 0; st < KS; ++st) {
           const float* kr = Ks + (size_t)j * KSTR + st * 16 + 2 * lt;
           const float2 k0 = *reinterpret_cast<const float2*>(kr);
