@@ -83,6 +83,24 @@ def test_failed_probes_back_off_and_an_accepting_probe_resets():
     assert n == 5
 
 
+def test_backoff_with_two_windows_in_flight():
+    """Windows complete in the order they were chosen; with two in flight the choice of window
+    k + 1 comes before the observation of window k, and a probe's own window still decides."""
+    c = W.Controller([1, 4], [100.0, 110.0])
+    for _ in range(20):
+        c.observe(4, [st(0, 0, 1)] * 4)
+    inflight = [c.choose(), c.choose()]
+    gaps, last = [], 0
+    for k in range(3, 400):
+        w = inflight.pop(0)
+        c.observe(w, [st(0, 0, 1)])                      # nothing is ever accepted
+        inflight.append(c.choose())
+        if inflight[-1] == 4:
+            gaps.append(k - last)
+            last = k
+    assert gaps[1:5] == [10, 20, 40, 64]
+
+
 def test_cost_moving_average():
     c = W.Controller([1, 4], [100.0, 200.0])
     c.observe(4, [st(1, 1)] * 4, interval_us=4 * 120.0)
