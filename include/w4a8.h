@@ -428,7 +428,9 @@ w4a8_status w4a8_session_copy_kv(w4a8_session* s, int layer, int slot0, int n, f
  * Width controller [P1 Feedback Control of Speculation Width], host only.
  * Chooses N maximising E[tokens per step | N] / T(N), where E is estimated from the
  * recent best match lengths and the acceptance observed per (width, match length);
- * probes a wider tree after a run of width-1 windows (spacing set by the costs);
+ * probes a wider tree after a run of width-1 windows (spacing set by the costs, doubled
+ * up to 64 windows after each probe window that accepts no draft, reset by one that does;
+ * windows must be observed in the order they were chosen);
  * refines T(N) with an exponential moving average of the device-measured window
  * completion intervals.
  * ---------------------------------------------------------------------------- */
