@@ -748,13 +748,12 @@ __global__ void __maxnreg__(168)
   if (!MERGE) return;
   consumers_sync();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned t = atomicAdd(tickets + kh, 1u);
+    // release (after the barrier: this CTA's partials) and acquire (the other splits') at GPU
+    // scope in one read-modify-write
+    unsigned t;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(tickets + kh) : "memory");
     const unsigned last = (t == (unsigned)(nsa - 1)) ? 1u : 0u;
-    if (last) {
-      __threadfence();
-      tickets[kh] = 0u;
-    }
+    if (last) tickets[kh] = 0u;  // read again only by a later launch
     s_last = last;
   }
   consumers_sync();
